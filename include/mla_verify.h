@@ -1,0 +1,164 @@
+/*
+ * mla_verify.h -- C ABI of the GB300 (sm_103a) MLA speculative-verify attention library.
+ *
+ * The operation ("The Occupancy Epiphany: How a CUDA Kernel Designer Discovered
+ * That GPU Utilization Trumps Memory Bandwidth", section "Context: The Problem
+ * and the Stakes"; "The Occupancy Probe", section "The Scene: What Came Before"):
+ * for every stream b, draft t < q_len and head h,
+ *
+ *     n = seq_lens[b], p = n - q_len                  (the drafts are the last q_len keys)
+ *     key j (0 <= j < n) is visible to draft t iff j < p, or mask[b,t,j-p] != 0
+ *     s_j   = scale * sum_{d<576} q[b,t,h,d] * kv[slot_table[b,j], d]
+ *     lse   = ln sum_{visible j} exp(s_j)
+ *     out[d] = sum_{visible j} exp(s_j - lse) * kv[slot_table[b,j], d]      (d < 512)
+ *
+ * i.e. masked softmax(Q K^T * scale) V of Multi-head Latent Attention in absorbed
+ * form: a 576-d query (512 latent + 64 rope) against 576-d latent KV rows whose
+ * first 512 dims double as V, over a page_size=1 paged cache.  The draft mask
+ * carries a causal chain or a draft tree ("The Occupancy Epiphany: How One
+ * Environment Variable Unlocked 3x Throughput ...", section "The Broader
+ * Context").  A draft that sees no key gets out = 0 and lse = -inf.
+ *
+ * The work is split along the keys (KV split, "flash decode"): split s writes a
+ * normalised partial output and its log-sum-exp, and a combine merges them
+ * ("The Occupancy Epiphany: How One Environment Variable ...", sections "The
+ * Occupancy Revelation" and "Output Knowledge Created").
+ *
+ * Conventions for every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller; the library keeps
+ *    none of them after the call returns and allocates no device memory.
+ *  - Work is enqueued on `stream` (NULL = the legacy default stream).  No entry
+ *    point synchronises except mla_verify_status(), which says so.
+ *  - Return value: MLA_OK (0) or a negative mla_status.  Argument errors are
+ *    detected on the host before anything is enqueued.  Errors that only the
+ *    device can see (a slot index outside [0, n_pool), a seq_len outside
+ *    [q_len, slot_stride], a bounded wait that expired) set bits of a per-device
+ *    status word, read with mla_verify_status(); the kernel never reads outside
+ *    its buffers because of them (it substitutes pool row 0 for a bad slot and
+ *    writes out = 0, lse = NaN for a stream with a bad length).
+ *  - Layouts are dense row-major C arrays with the shapes given below; bf16 is
+ *    IEEE bfloat16 bit patterns (uint16).
+ */
+#ifndef MLA_VERIFY_H
+#define MLA_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* mla_stream_t;
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_NULL = -1,       /* a required pointer is NULL */
+    MLA_ERR_SHAPE = -2,      /* a size is outside the supported range */
+    MLA_ERR_ALIGN = -3,      /* a pointer is not aligned as required */
+    MLA_ERR_WORKSPACE = -4,  /* workspace NULL or smaller than mla_verify_workspace_bytes() */
+    MLA_ERR_NSPLIT = -5,     /* nsplit outside [0, MLA_MAX_NSPLIT] */
+    MLA_ERR_LAUNCH = -6,     /* the CUDA launch failed (cudaGetLastError) */
+    MLA_ERR_DEVICE = -7,     /* no usable sm_103 device / CUDA runtime error */
+    MLA_ERR_ARG = -8         /* any other invalid argument (e.g. non-finite scale) */
+} mla_status;
+
+/* Device status word bits (mla_verify_status). */
+#define MLA_DEV_BAD_SLOT 0x1u  /* a slot index outside [0, n_pool); pool row 0 was read instead */
+#define MLA_DEV_BAD_LEN 0x2u   /* a seq_len outside [q_len, slot_stride]; that stream was skipped */
+#define MLA_DEV_TIMEOUT 0x4u   /* a bounded device-side wait expired; the CTA gave up */
+
+/* Supported ranges. */
+#define MLA_D_QK 576           /* query / key width: 512 latent + 64 rope */
+#define MLA_D_V 512            /* value / output width */
+#define MLA_MAX_Q_LEN 16
+#define MLA_MAX_HEADS 128
+#define MLA_MAX_NSPLIT 1024
+
+/*
+ * Bytes of workspace that mla_verify_attn() needs for `nsplit` key splits
+ * (nsplit >= 1; 0 when nsplit == 1, which needs none).  Layout, 256-byte
+ * aligned sections: partial outputs fp32 [B, q_len, H, nsplit, 512], then
+ * partial log-sum-exps fp32 [B, q_len, H, nsplit].  Pure host function.
+ */
+size_t mla_verify_workspace_bytes(int B, int q_len, int H, int nsplit);
+
+/*
+ * The split count that mla_verify_attn() uses when called with nsplit = 0:
+ * deterministic in (B, q_len, H, max_seq = slot_stride, num_sms, ws_bytes),
+ * chosen so that the launch fills the SMs ("The Occupancy Epiphany: How One
+ * Environment Variable ...", section "The Occupancy Revelation": grid =
+ * streams x q_len x heads x NSPLIT blocks, and too few waves starve the GPU)
+ * while keeping every split at least a few key tiles long, and never more
+ * splits than the workspace holds.  Pure host function.
+ */
+int mla_verify_auto_nsplit(int B, int q_len, int H, int max_seq, int num_sms, size_t ws_bytes);
+
+/*
+ * Verify attention (definition above).
+ *   q          bf16 [B, q_len, H, 576], 16-byte aligned
+ *   kv_cache   bf16 [n_pool, 576] latent KV pool, 16-byte aligned; row = 512 latent | 64 rope
+ *   slot_table int32 [B, slot_stride]: pool row of key j of stream b; the drafts are
+ *              keys seq_lens[b]-q_len .. seq_lens[b]-1, in draft order
+ *   seq_lens   int32 [B], keys per stream (prefix + q_len); q_len <= seq_lens[b] <= slot_stride
+ *   draft_mask uint8 [B, q_len, q_len] (mask[b,t,i] != 0: draft t sees draft i) or NULL
+ *              for a causal chain (draft t sees drafts 0..t)
+ *   scale      multiplies every score (e.g. 1/sqrt(192))
+ *   out        fp32 [B, q_len, H, 512], 16-byte aligned
+ *   lse        fp32 [B, q_len, H], natural log of sum exp(scaled scores)
+ *   nsplit     0 = automatic (mla_verify_auto_nsplit), else 1..MLA_MAX_NSPLIT key splits
+ *   workspace  device scratch of ws_bytes >= mla_verify_workspace_bytes(B,q_len,H,nsplit_used),
+ *              256-byte aligned; may be NULL when the split count used is 1
+ * Limits: 1 <= q_len <= 16, 1 <= H <= 128, 0 <= B <= 65535 (B == 0 is a no-op), n_pool >= 1.
+ */
+int mla_verify_attn(const void* q, const void* kv_cache, int64_t n_pool,
+                    const int32_t* slot_table, int slot_stride, const int32_t* seq_lens,
+                    const uint8_t* draft_mask, int B, int q_len, int H, float scale,
+                    float* out, float* lse, int nsplit, void* workspace, size_t ws_bytes,
+                    mla_stream_t stream);
+
+/*
+ * The split stage of mla_verify_attn() alone: with nsplit >= 2 it writes the
+ * partial outputs and log-sum-exps into `workspace` (layout of
+ * mla_verify_workspace_bytes) and enqueues nothing else; nsplit must be given
+ * explicitly (>= 1); with nsplit == 1 it writes out/lse directly, like
+ * mla_verify_attn.  Split s of a stream with n keys covers keys
+ * [s*c, (s+1)*c) intersected with [0, n), where c = ceil(n / nsplit) rounded up
+ * to a multiple of 32; trailing splits may be empty (lse = -inf, out = 0).
+ * mla_verify_partials() followed by mla_verify_combine() on the workspace
+ * sections is exactly mla_verify_attn().
+ */
+int mla_verify_partials(const void* q, const void* kv_cache, int64_t n_pool,
+                        const int32_t* slot_table, int slot_stride, const int32_t* seq_lens,
+                        const uint8_t* draft_mask, int B, int q_len, int H, float scale,
+                        float* out, float* lse, int nsplit, void* workspace, size_t ws_bytes,
+                        mla_stream_t stream);
+
+/*
+ * Log-sum-exp merge of KV-split partials for n_rows = B*q_len*H rows:
+ *   part_out fp32 [n_rows, S, 512] (each split's normalised output), 16-byte aligned
+ *   part_lse fp32 [n_rows, S] (each split's log-sum-exp; -inf for an empty split)
+ *   lse = ln sum_s exp(part_lse[s]);  out = sum_s exp(part_lse[s] - lse) * part_out[s]
+ * A row whose splits are all empty gets out = 0, lse = -inf.  1 <= S <= MLA_MAX_NSPLIT.
+ */
+int mla_verify_combine(const float* part_out, const float* part_lse, int B, int q_len, int H,
+                       int S, float* out, float* lse, mla_stream_t stream);
+
+/*
+ * Reads (and with clear != 0 resets) the calling device's status word of
+ * MLA_DEV_* bits.  SYNCHRONISES `stream`.  Returns MLA_OK or MLA_ERR_DEVICE.
+ */
+int mla_verify_status(mla_stream_t stream, uint32_t* device_status, int clear);
+
+/* Static string for an mla_status value. */
+const char* mla_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int mla_verify_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_VERIFY_H */

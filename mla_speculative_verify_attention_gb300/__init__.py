@@ -1,0 +1,197 @@
+"""GB300 (sm_103a) MLA speculative-verify attention.
+
+A thin ctypes binding over the C ABI of ``include/mla_verify.h``
+(``_lib/libmla_verify_gb300.so``).  PyTorch supplies device memory and streams;
+every step of the computation runs in the library's CUDA kernels.  There is no
+CPU fallback: if the library is missing, ``load()`` raises.
+
+Build it with ``python -m mla_speculative_verify_attention_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+D_QK = 576
+D_V = 512
+MAX_Q_LEN = 16
+MAX_HEADS = 128
+MAX_NSPLIT = 1024
+
+MLA_OK = 0
+STATUS_NAMES = {0: "MLA_OK", -1: "MLA_ERR_NULL", -2: "MLA_ERR_SHAPE", -3: "MLA_ERR_ALIGN",
+                -4: "MLA_ERR_WORKSPACE", -5: "MLA_ERR_NSPLIT", -6: "MLA_ERR_LAUNCH",
+                -7: "MLA_ERR_DEVICE", -8: "MLA_ERR_ARG"}
+DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
+
+EXPORTS = ("mla_verify_workspace_bytes", "mla_verify_auto_nsplit", "mla_verify_attn",
+           "mla_verify_partials", "mla_verify_combine", "mla_verify_status",
+           "mla_status_string", "mla_verify_version")
+
+_lib = None
+
+
+class MlaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code} ({STATUS_NAMES.get(code, 'unknown')})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing "
+                           "(run python -m mla_speculative_verify_attention_gb300.build)")
+    L = ctypes.CDLL(path)
+    P, I, I64, SZ, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    L.mla_verify_workspace_bytes.argtypes = [I, I, I, I]
+    L.mla_verify_workspace_bytes.restype = SZ
+    L.mla_verify_auto_nsplit.argtypes = [I, I, I, I, I, SZ]
+    L.mla_verify_auto_nsplit.restype = I
+    sig = [P, P, I64, P, I, P, P, I, I, I, F, P, P, I, P, SZ, P]
+    for fn in ("mla_verify_attn", "mla_verify_partials"):
+        getattr(L, fn).argtypes = sig
+        getattr(L, fn).restype = I
+    L.mla_verify_combine.argtypes = [P, P, I, I, I, I, P, P, P]
+    L.mla_verify_combine.restype = I
+    L.mla_verify_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I]
+    L.mla_verify_status.restype = I
+    L.mla_status_string.argtypes = [I]
+    L.mla_status_string.restype = ctypes.c_char_p
+    L.mla_verify_version.argtypes = []
+    L.mla_verify_version.restype = I
+    _lib = L
+    return L
+
+
+def _check(fn: str, rc: int):
+    if rc != MLA_OK:
+        raise MlaError(fn, rc)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def workspace_bytes(B: int, q_len: int, H: int, nsplit: int) -> int:
+    return int(load().mla_verify_workspace_bytes(B, q_len, H, nsplit))
+
+
+def auto_nsplit(B: int, q_len: int, H: int, max_seq: int, num_sms: int, ws_bytes: int) -> int:
+    return int(load().mla_verify_auto_nsplit(B, q_len, H, max_seq, num_sms, ws_bytes))
+
+
+def num_sms(device=None) -> int:
+    return torch.cuda.get_device_properties(device if device is not None else torch.cuda.current_device()).multi_processor_count
+
+
+def _check_verify_tensors(q, kv_cache, slot_table, seq_lens, draft_mask):
+    if q.dtype != torch.bfloat16 or kv_cache.dtype != torch.bfloat16:
+        raise TypeError("q and kv_cache must be bfloat16")
+    if q.dim() != 4 or q.shape[-1] != D_QK or kv_cache.dim() != 2 or kv_cache.shape[1] != D_QK:
+        raise ValueError("q must be [B, q_len, H, 576] and kv_cache [n_pool, 576]")
+    if slot_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("slot_table and seq_lens must be int32")
+    for t in (q, kv_cache, slot_table, seq_lens) + ((draft_mask,) if draft_mask is not None else ()):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    if draft_mask is not None and draft_mask.dtype != torch.uint8:
+        raise TypeError("draft_mask must be uint8")
+
+
+def verify_attn(q: torch.Tensor, kv_cache: torch.Tensor, slot_table: torch.Tensor, seq_lens: torch.Tensor,
+                draft_mask: Optional[torch.Tensor], scale: float, *, out: Optional[torch.Tensor] = None,
+                lse: Optional[torch.Tensor] = None, nsplit: int = 0, workspace: Optional[torch.Tensor] = None,
+                stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """mla_verify_attn: out [B, q_len, H, 512] fp32 and lse [B, q_len, H] fp32.
+
+    ``workspace`` is a byte (uint8) CUDA tensor; when omitted, one sized for the
+    split count in use is allocated here (by torch, outside the library)."""
+    L = load()
+    _check_verify_tensors(q, kv_cache, slot_table, seq_lens, draft_mask)
+    B, q_len, H, _ = q.shape
+    if out is None:
+        out = torch.empty((B, q_len, H, D_V), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, q_len, H), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        ns = nsplit if nsplit > 0 else auto_nsplit(B, q_len, H, slot_table.shape[1], num_sms(q.device), 1 << 62)
+        workspace = torch.empty(max(workspace_bytes(B, q_len, H, ns), 256), dtype=torch.uint8, device=q.device)
+    rc = L.mla_verify_attn(_ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(slot_table), slot_table.shape[1],
+                           _ptr(seq_lens), _ptr(draft_mask), B, q_len, H, float(scale), _ptr(out), _ptr(lse),
+                           nsplit, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("mla_verify_attn", rc)
+    return out, lse
+
+
+def verify_partials(q, kv_cache, slot_table, seq_lens, draft_mask, scale, *, nsplit: int,
+                    workspace: torch.Tensor, out: Optional[torch.Tensor] = None,
+                    lse: Optional[torch.Tensor] = None, stream=None):
+    """mla_verify_partials: the split stage alone (nsplit >= 1 explicit).  Returns
+    (part_out [B*q_len*H, nsplit, 512], part_lse [B*q_len*H, nsplit]) views of the
+    workspace when nsplit > 1, else (out, lse)."""
+    L = load()
+    _check_verify_tensors(q, kv_cache, slot_table, seq_lens, draft_mask)
+    B, q_len, H, _ = q.shape
+    if out is None:
+        out = torch.empty((B, q_len, H, D_V), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, q_len, H), dtype=torch.float32, device=q.device)
+    rc = L.mla_verify_partials(_ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(slot_table), slot_table.shape[1],
+                               _ptr(seq_lens), _ptr(draft_mask), B, q_len, H, float(scale), _ptr(out), _ptr(lse),
+                               nsplit, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("mla_verify_partials", rc)
+    if nsplit == 1:
+        return out, lse
+    return workspace_views(workspace, B, q_len, H, nsplit)
+
+
+def workspace_views(workspace: torch.Tensor, B: int, q_len: int, H: int, nsplit: int):
+    """(part_out [rows, nsplit, 512], part_lse [rows, nsplit]) float32 views of a workspace."""
+    rows = B * q_len * H
+    n_out = rows * nsplit * D_V * 4
+    off = (n_out + 255) // 256 * 256
+    po = workspace[:n_out].view(torch.float32).view(rows, nsplit, D_V)
+    pl = workspace[off:off + rows * nsplit * 4].view(torch.float32).view(rows, nsplit)
+    return po, pl
+
+
+def verify_combine(part_out: torch.Tensor, part_lse: torch.Tensor, B: int, q_len: int, H: int, *,
+                   out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, stream=None):
+    """mla_verify_combine: part_out [B*q_len*H, S, 512], part_lse [B*q_len*H, S] (fp32)."""
+    L = load()
+    S = part_lse.shape[-1]
+    if out is None:
+        out = torch.empty((B, q_len, H, D_V), dtype=torch.float32, device=part_out.device)
+    if lse is None:
+        lse = torch.empty((B, q_len, H), dtype=torch.float32, device=part_out.device)
+    rc = L.mla_verify_combine(_ptr(part_out), _ptr(part_lse), B, q_len, H, S, _ptr(out), _ptr(lse), _stream(stream))
+    _check("mla_verify_combine", rc)
+    return out, lse
+
+
+def device_status(stream=None, clear: bool = True) -> int:
+    """Reads (and clears) the device status word; synchronises the stream."""
+    v = ctypes.c_uint32(0)
+    _check("mla_verify_status", load().mla_verify_status(_stream(stream), ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)

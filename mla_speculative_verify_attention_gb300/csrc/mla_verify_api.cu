@@ -1,0 +1,294 @@
+// Host side of the C ABI declared in include/mla_verify.h: argument checks,
+// the split-count policy, the per-device status word, and the log-sum-exp
+// combine kernel that merges KV-split partials.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/mla_verify.h"
+#include "internal.cuh"
+
+namespace mla {
+
+// Per-device status word of MLA_DEV_* bits (sticky until mla_verify_status clears it).
+__device__ unsigned g_status;
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+unsigned* g_status_ptr[MAX_DEVICES];
+int g_num_sms[MAX_DEVICES];
+int g_arch_ok[MAX_DEVICES];      // 0 unknown, 1 sm_103, -1 other
+
+// Device properties and the status word's device address for the current device.
+int device_state(int* dev_out, unsigned** status, int* num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return MLA_ERR_DEVICE;
+    if (g_arch_ok[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MLA_ERR_DEVICE;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return MLA_ERR_DEVICE;
+        g_status_ptr[dev] = static_cast<unsigned*>(p);
+        g_num_sms[dev] = sms;
+        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (g_arch_ok[dev] != 1) return MLA_ERR_DEVICE;
+    if (dev_out) *dev_out = dev;
+    if (status) *status = g_status_ptr[dev];
+    if (num_sms) *num_sms = g_num_sms[dev];
+    return MLA_OK;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------------------------
+// Combine: one CTA of 128 threads per (row, 32 output dims).  Thread (sg, dv)
+// with sg = tid / 8, dv = tid % 8 accumulates the float4 dv of the chunk over
+// splits s = sg, sg + 16, ...; the 16 partial sums are added in shared memory.
+// ---------------------------------------------------------------------------
+constexpr int CB_THREADS = 128;
+constexpr int CB_DIMS = 32;
+
+__device__ __forceinline__ float block_max128(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    __syncthreads();
+    return v;
+}
+__device__ __forceinline__ float block_sum128(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = (red[0] + red[1]) + (red[2] + red[3]);
+    __syncthreads();
+    return v;
+}
+
+__global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __restrict__ part_out,
+                                                             const float* __restrict__ part_lse, int S,
+                                                             float* __restrict__ out, float* __restrict__ lse) {
+    __shared__ float red[4];
+    __shared__ float4 acc_s[16][8];
+    const int tid = threadIdx.x;
+    const int chunk = blockIdx.y;
+    const long long row = blockIdx.x;
+    const float* pl = part_lse + row * S;
+
+    float mx = -INFINITY, bad = 0.f;
+    for (int s = tid; s < S; s += CB_THREADS) {
+        float v = pl[s];
+        if (v != v) bad = 1.f;
+        mx = fmaxf(mx, v);
+    }
+    mx = block_max128(mx, red);
+    bad = block_max128(bad, red);
+    float* o = out + row * D_V + chunk * CB_DIMS;
+    if (bad != 0.f || mx == -INFINITY) {          // malformed stream or no visible key
+        if (tid < 8) reinterpret_cast<float4*>(o)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (chunk == 0 && tid == 0) lse[row] = bad != 0.f ? __int_as_float(0x7fc00000) : -INFINITY;
+        return;
+    }
+    float z = 0.f;
+    for (int s = tid; s < S; s += CB_THREADS) z += expf(pl[s] - mx);
+    z = block_sum128(z, red);
+    const float L = mx + logf(z);
+
+    const int sg = tid >> 3, dv = tid & 7;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = sg; s < S; s += 16) {
+        float w = expf(pl[s] - L);
+        if (w == 0.f) continue;
+        float4 v = reinterpret_cast<const float4*>(part_out + (row * S + s) * D_V + chunk * CB_DIMS)[dv];
+        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+    }
+    acc_s[sg][dv] = acc;
+    __syncthreads();
+    if (tid < 8) {
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {
+            float4 v = acc_s[g][tid];
+            r.x += v.x; r.y += v.y; r.z += v.z; r.w += v.w;
+        }
+        reinterpret_cast<float4*>(o)[tid] = r;
+    }
+    if (chunk == 0 && tid == 0) lse[row] = L;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* part_out, const float* part_lse, long long n_rows, int S,
+                           float* out, float* lse, cudaStream_t stream) {
+    if (n_rows <= 0) return cudaSuccess;
+    dim3 grid((unsigned)n_rows, D_V / CB_DIMS);
+    combine_kernel<<<grid, CB_THREADS, 0, stream>>>(part_out, part_lse, S, out, lse);
+    return cudaGetLastError();
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+namespace {
+
+// Tiling of the split kernel that the split-count policy plans for.
+constexpr int PLAN_ROWS_PER_CTA = SIMT_ROWS;
+constexpr int PLAN_CTAS_PER_SM = 2;
+constexpr int PLAN_MIN_KEYS_PER_SPLIT = 128;
+
+int check_verify_args(const void* q, const void* kv, int64_t n_pool, const int32_t* slot, int slot_stride,
+                      const int32_t* seq_lens, int B, int q_len, int H, float scale, const float* out,
+                      const float* lse, int nsplit) {
+    if (B < 0 || B > 65535 || q_len < 1 || q_len > MLA_MAX_Q_LEN || H < 1 || H > MLA_MAX_HEADS) return MLA_ERR_SHAPE;
+    if (nsplit < 0 || nsplit > MLA_MAX_NSPLIT) return MLA_ERR_NSPLIT;
+    if (B == 0) return MLA_OK;
+    if (!q || !kv || !slot || !seq_lens || !out || !lse) return MLA_ERR_NULL;
+    if (n_pool < 1 || slot_stride < q_len) return MLA_ERR_SHAPE;
+    if (!isfinite(scale)) return MLA_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(slot, 4) ||
+        !aligned(seq_lens, 4) || !aligned(lse, 4))
+        return MLA_ERR_ALIGN;
+    return MLA_OK;
+}
+
+int run_verify(bool combine, const void* q, const void* kv, int64_t n_pool, const int32_t* slot,
+               int slot_stride, const int32_t* seq_lens, const uint8_t* mask, int B, int q_len, int H,
+               float scale, float* out, float* lse, int nsplit, void* ws, size_t ws_bytes,
+               cudaStream_t stream) {
+    int rc = check_verify_args(q, kv, n_pool, slot, slot_stride, seq_lens, B, q_len, H, scale, out, lse, nsplit);
+    if (rc != MLA_OK) return rc;
+    if (!combine && nsplit == 0) return MLA_ERR_NSPLIT;
+    if (B == 0) return MLA_OK;
+    unsigned* status = nullptr;
+    int num_sms = 0;
+    rc = device_state(nullptr, &status, &num_sms);
+    if (rc != MLA_OK) return rc;
+    int ns = nsplit > 0 ? nsplit : mla_verify_auto_nsplit(B, q_len, H, slot_stride, num_sms, ws ? ws_bytes : 0);
+    const long long rows = (long long)B * q_len * H;
+    VerifyArgs a;
+    memset(&a, 0, sizeof a);
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.kv = static_cast<const __nv_bfloat16*>(kv);
+    a.n_pool = n_pool;
+    a.slot = slot;
+    a.slot_stride = slot_stride;
+    a.seq_lens = seq_lens;
+    a.mask = mask;
+    a.B = B; a.q_len = q_len; a.H = H;
+    a.scale = scale;
+    a.out = out; a.lse = lse;
+    a.nsplit = ns;
+    a.status = status;
+    if (ns > 1) {
+        size_t need = mla_verify_workspace_bytes(B, q_len, H, ns);
+        if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+        if (!aligned(ws, 256)) return MLA_ERR_ALIGN;
+        a.part_out = static_cast<float*>(ws);
+        a.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)rows * ns * D_V * 4));
+    }
+    if (launch_verify_simt(a, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+    if (combine && ns > 1 && launch_combine(a.part_out, a.part_lse, rows, ns, out, lse, stream) != cudaSuccess)
+        return MLA_ERR_LAUNCH;
+    return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mla_verify_workspace_bytes(int B, int q_len, int H, int nsplit) {
+    if (B < 0 || q_len < 1 || H < 1 || nsplit < 1 || nsplit == 1) return 0;
+    size_t rows = (size_t)B * q_len * H;
+    return align256(rows * nsplit * D_V * 4) + align256(rows * nsplit * 4);
+}
+
+int mla_verify_auto_nsplit(int B, int q_len, int H, int max_seq, int num_sms, size_t ws_bytes) {
+    if (B <= 0 || q_len < 1 || H < 1 || max_seq < 1 || num_sms < 1) return 1;
+    const long long tiles = ((long long)q_len * H + PLAN_ROWS_PER_CTA - 1) / PLAN_ROWS_PER_CTA;
+    const long long ctas = (long long)B * tiles;
+    const long long target = (long long)num_sms * PLAN_CTAS_PER_SM;
+    long long ns = (target + ctas - 1) / ctas;
+    const long long by_len = (max_seq + PLAN_MIN_KEYS_PER_SPLIT - 1) / PLAN_MIN_KEYS_PER_SPLIT;
+    if (ns > by_len) ns = by_len;
+    if (ns > MLA_MAX_NSPLIT) ns = MLA_MAX_NSPLIT;
+    if (ns < 1) ns = 1;
+    while (ns > 1 && mla_verify_workspace_bytes(B, q_len, H, (int)ns) > ws_bytes) --ns;
+    return (int)ns;
+}
+
+int mla_verify_attn(const void* q, const void* kv_cache, int64_t n_pool, const int32_t* slot_table,
+                    int slot_stride, const int32_t* seq_lens, const uint8_t* draft_mask, int B, int q_len,
+                    int H, float scale, float* out, float* lse, int nsplit, void* workspace, size_t ws_bytes,
+                    mla_stream_t stream) {
+    return run_verify(true, q, kv_cache, n_pool, slot_table, slot_stride, seq_lens, draft_mask, B, q_len, H,
+                      scale, out, lse, nsplit, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_verify_partials(const void* q, const void* kv_cache, int64_t n_pool, const int32_t* slot_table,
+                        int slot_stride, const int32_t* seq_lens, const uint8_t* draft_mask, int B, int q_len,
+                        int H, float scale, float* out, float* lse, int nsplit, void* workspace,
+                        size_t ws_bytes, mla_stream_t stream) {
+    return run_verify(false, q, kv_cache, n_pool, slot_table, slot_stride, seq_lens, draft_mask, B, q_len, H,
+                      scale, out, lse, nsplit, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_verify_combine(const float* part_out, const float* part_lse, int B, int q_len, int H, int S, float* out,
+                       float* lse, mla_stream_t stream) {
+    if (B < 0 || q_len < 1 || H < 1 || (long long)B * q_len * H > 0x7fffffffLL) return MLA_ERR_SHAPE;
+    if (S < 1 || S > MLA_MAX_NSPLIT) return MLA_ERR_NSPLIT;
+    if (B == 0) return MLA_OK;
+    if (!part_out || !part_lse || !out || !lse) return MLA_ERR_NULL;
+    if (!aligned(part_out, 16) || !aligned(out, 16) || !aligned(part_lse, 4) || !aligned(lse, 4))
+        return MLA_ERR_ALIGN;
+    int rc = device_state(nullptr, nullptr, nullptr);
+    if (rc != MLA_OK) return rc;
+    long long rows = (long long)B * q_len * H;
+    if (launch_combine(part_out, part_lse, rows, S, out, lse, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MLA_ERR_LAUNCH;
+    return MLA_OK;
+}
+
+int mla_verify_status(mla_stream_t stream, uint32_t* device_status, int clear) {
+    if (!device_status) return MLA_ERR_NULL;
+    unsigned* st = nullptr;
+    int rc = device_state(nullptr, &st, nullptr);
+    if (rc != MLA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned v = 0;
+    if (cudaMemcpyAsync(&v, st, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MLA_ERR_DEVICE;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_DEVICE;
+    if (clear) {
+        if (cudaMemsetAsync(st, 0, sizeof(unsigned), s) != cudaSuccess) return MLA_ERR_DEVICE;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_DEVICE;
+    }
+    *device_status = v;
+    return MLA_OK;
+}
+
+const char* mla_status_string(int status) {
+    switch (status) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_NULL: return "null pointer";
+        case MLA_ERR_SHAPE: return "shape out of range";
+        case MLA_ERR_ALIGN: return "misaligned pointer";
+        case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+        case MLA_ERR_NSPLIT: return "nsplit out of range";
+        case MLA_ERR_LAUNCH: return "kernel launch failed";
+        case MLA_ERR_DEVICE: return "no usable sm_103 device or CUDA runtime error";
+        case MLA_ERR_ARG: return "invalid argument";
+        default: return "unknown status";
+    }
+}
+
+int mla_verify_version(void) { return 100; }
+
+}  // extern "C"

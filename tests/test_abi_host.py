@@ -1,0 +1,107 @@
+"""The C-ABI library on the host: it loads, exports every symbol include/*.h declares,
+and its pure-host functions and argument checks behave as documented.  Nothing here
+launches a kernel or touches device memory: every call either is a pure host function
+or fails argument validation before the library makes any CUDA call."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mla_speculative_verify_attention_gb300 import build
+    build.build()
+    import mla_speculative_verify_attention_gb300 as mv
+    return mv.load()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(mla_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "mla_verify_attn" in names and "mla_verify_combine" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.mla_verify_version() >= 100
+    assert lib.mla_status_string(0) == b"ok"
+    assert lib.mla_status_string(-4).startswith(b"workspace")
+
+
+def test_workspace_bytes(lib):
+    ws = lib.mla_verify_workspace_bytes
+    assert ws(1, 9, 8, 1) == 0
+    rows, S = 72, 64
+    out_b = rows * S * 512 * 4
+    lse_b = (rows * S * 4 + 255) // 256 * 256
+    assert ws(1, 9, 8, S) == (out_b + 255) // 256 * 256 + lse_b
+    assert ws(-1, 9, 8, 4) == 0 and ws(1, 0, 8, 4) == 0
+
+
+def test_auto_nsplit_policy(lib):
+    f = lib.mla_verify_auto_nsplit
+    big = 1 << 40
+    for args in [(1, 9, 8, 16393, 152), (1, 9, 64, 4105, 152), (8, 9, 8, 46089, 152), (1, 9, 8, 265, 152)]:
+        ns = f(*args, big)
+        assert 1 <= ns <= 1024
+        assert ns * 128 <= args[3] + 127                  # every split keeps >= ~128 keys
+    # deterministic, and capped by the workspace the caller provides
+    assert f(1, 9, 8, 65545, 152, big) == f(1, 9, 8, 65545, 152, big)
+    one = lib.mla_verify_workspace_bytes(1, 9, 8, 2)
+    assert f(1, 9, 8, 65545, 152, one) == 2
+    assert f(1, 9, 8, 65545, 152, 0) == 1
+
+
+def _call_attn(lib, **kw):
+    a = dict(q=16, kv=16, n_pool=10, slot=16, stride=16, seq=16, mask=None, B=1, q_len=9, H=8, scale=0.1,
+             out=16, lse=16, nsplit=1, ws=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.mla_verify_attn(P(a["q"]), P(a["kv"]), a["n_pool"], P(a["slot"]), a["stride"], P(a["seq"]),
+                               P(a["mask"]), a["B"], a["q_len"], a["H"], a["scale"], P(a["out"]), P(a["lse"]),
+                               a["nsplit"], P(a["ws"]), a["ws_bytes"], P(a["stream"]))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(kv=None), -1), (dict(slot=None), -1), (dict(out=None), -1),
+    (dict(q_len=0), -2), (dict(q_len=17), -2), (dict(H=0), -2), (dict(H=129), -2),
+    (dict(stride=8), -2), (dict(n_pool=0), -2),
+    (dict(q=24), -3), (dict(out=20), -3), (dict(slot=18), -3),
+    (dict(nsplit=-1), -5), (dict(nsplit=1025), -5),
+    (dict(scale=float("inf")), -8),
+])
+def test_argument_errors_before_any_cuda_call(lib, kw, code):
+    assert _call_attn(lib, **kw) == code
+
+
+def test_zero_streams_with_bad_pointers_is_ok(lib):
+    assert _call_attn(lib, B=0, q=None, kv=None) == 0
+
+
+def test_partials_needs_explicit_nsplit(lib):
+    P = ctypes.c_void_p
+    rc = lib.mla_verify_partials(P(16), P(16), 10, P(16), 16, P(16), None, 1, 9, 8, 0.1, P(16), P(16), 0, None, 0,
+                                 None)
+    assert rc == -5
+
+
+def test_combine_argument_errors(lib):
+    P = ctypes.c_void_p
+    assert lib.mla_verify_combine(None, P(16), 1, 9, 8, 4, P(16), P(16), None) == -1
+    assert lib.mla_verify_combine(P(16), P(16), 1, 9, 8, 0, P(16), P(16), None) == -5
+    assert lib.mla_verify_combine(P(16), P(16), 1, 0, 8, 4, P(16), P(16), None) == -2
+    assert lib.mla_verify_combine(P(8), P(16), 1, 9, 8, 4, P(16), P(16), None) == -3

@@ -146,6 +146,34 @@ int mla_verify_combine(const float* part_out, const float* part_lse, int B, int 
                        int S, float* out, float* lse, mla_stream_t stream);
 
 /*
+ * Verify attention without a caller-provided workspace, for callers that cannot
+ * allocate device memory: plugins hosted by a runtime that owns all device
+ * memory (a serving engine's caching allocator or a fixed arena that must not
+ * be bypassed) and latency-critical loops where cudaMalloc/cudaFree, which can
+ * synchronise the device or fail under memory pressure, are not allowed.  The
+ * pages have no counterpart of this entry point.
+ *
+ * Same arguments and result as mla_verify_attn() minus the workspace.  The
+ * KV-split partials go to a file-scope device array of MLA_STATIC_SCRATCH_BYTES
+ * that every GPU loading this library holds until the process exits; nothing
+ * is allocated per call (no cudaMalloc, no cudaFree, no allocating library
+ * routine).  With nsplit = 0 the split count is chosen to fit the array; an
+ * explicit nsplit whose partials need more than MLA_STATIC_SCRATCH_BYTES
+ * (mla_verify_workspace_bytes) returns MLA_ERR_WORKSPACE.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls on a device share the one array and it keeps
+ * the last call's contents (every call overwrites what it reads, so nothing
+ * needs clearing); calls whose GPU work overlaps -- on different streams, or
+ * from different host threads -- race on it and must be serialised by the caller.
+ */
+#define MLA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+int mla_verify_attn_static_scratch(const void* q, const void* kv_cache, int64_t n_pool,
+                                   const int32_t* slot_table, int slot_stride, const int32_t* seq_lens,
+                                   const uint8_t* draft_mask, int B, int q_len, int H, float scale,
+                                   float* out, float* lse, int nsplit, mla_stream_t stream);
+
+/*
  * Reads (and with clear != 0 resets) the calling device's status word of
  * MLA_DEV_* bits.  SYNCHRONISES `stream`.  Returns MLA_OK or MLA_ERR_DEVICE.
  */

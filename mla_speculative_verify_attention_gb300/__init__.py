@@ -32,7 +32,8 @@ DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = ("mla_verify_workspace_bytes", "mla_verify_auto_nsplit", "mla_verify_attn",
            "mla_verify_partials", "mla_verify_combine", "mla_verify_status",
-           "mla_status_string", "mla_verify_version")
+           "mla_status_string", "mla_verify_version", "mla_verify_attn_static_scratch")
+STATIC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
 
@@ -66,6 +67,8 @@ def load():
     for fn in ("mla_verify_attn", "mla_verify_partials"):
         getattr(L, fn).argtypes = sig
         getattr(L, fn).restype = I
+    L.mla_verify_attn_static_scratch.argtypes = [P, P, I64, P, I, P, P, I, I, I, F, P, P, I, P]
+    L.mla_verify_attn_static_scratch.restype = I
     L.mla_verify_combine.argtypes = [P, P, I, I, I, I, P, P, P]
     L.mla_verify_combine.restype = I
     L.mla_verify_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I]
@@ -141,6 +144,28 @@ def verify_attn(q: torch.Tensor, kv_cache: torch.Tensor, slot_table: torch.Tenso
                            _ptr(seq_lens), _ptr(draft_mask), B, q_len, H, float(scale), _ptr(out), _ptr(lse),
                            nsplit, _ptr(workspace), workspace.numel(), _stream(stream))
     _check("mla_verify_attn", rc)
+    return out, lse
+
+
+def verify_attn_static_scratch(q: torch.Tensor, kv_cache: torch.Tensor, slot_table: torch.Tensor,
+                               seq_lens: torch.Tensor, draft_mask: Optional[torch.Tensor], scale: float, *,
+                               out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                               nsplit: int = 0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """mla_verify_attn_static_scratch: verify attention whose split partials live in the
+    library's own static device array, for callers that cannot allocate device memory
+    (no workspace argument; the library allocates nothing).  Calls whose GPU work
+    overlaps share that array and race; the first call on a device sets it up."""
+    L = load()
+    _check_verify_tensors(q, kv_cache, slot_table, seq_lens, draft_mask)
+    B, q_len, H, _ = q.shape
+    if out is None:
+        out = torch.empty((B, q_len, H, D_V), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, q_len, H), dtype=torch.float32, device=q.device)
+    rc = L.mla_verify_attn_static_scratch(_ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(slot_table),
+                                          slot_table.shape[1], _ptr(seq_lens), _ptr(draft_mask), B, q_len, H,
+                                          float(scale), _ptr(out), _ptr(lse), nsplit, _stream(stream))
+    _check("mla_verify_attn_static_scratch", rc)
     return out, lse
 
 

@@ -141,8 +141,8 @@ using namespace mla;
 namespace {
 
 // Tiling of the split kernel that the split-count policy plans for.
-constexpr int PLAN_ROWS_PER_CTA = SIMT_ROWS;
-constexpr int PLAN_CTAS_PER_SM = 2;
+constexpr int PLAN_ROWS_PER_CTA = TC_MAX_ROWS;
+constexpr int PLAN_CTAS_PER_SM = 1;
 constexpr int PLAN_MIN_KEYS_PER_SPLIT = 128;
 
 int check_verify_args(const void* q, const void* kv, int64_t n_pool, const int32_t* slot, int slot_stride,
@@ -195,7 +195,7 @@ int run_verify(bool combine, const void* q, const void* kv, int64_t n_pool, cons
         a.part_out = static_cast<float*>(ws);
         a.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)rows * ns * D_V * 4));
     }
-    if (launch_verify_simt(a, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+    if (launch_verify_tc(a, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
     if (combine && ns > 1 && launch_combine(a.part_out, a.part_lse, rows, ns, out, lse, stream) != cudaSuccess)
         return MLA_ERR_LAUNCH;
     return MLA_OK;

@@ -67,7 +67,7 @@ typedef enum {
 /* Device status word bits (mla_verify_status). */
 #define MLA_DEV_BAD_SLOT 0x1u  /* a slot index outside [0, n_pool); pool row 0 was read instead */
 #define MLA_DEV_BAD_LEN 0x2u   /* a seq_len outside [q_len, slot_stride]; that stream was skipped */
-#define MLA_DEV_TIMEOUT 0x4u   /* a bounded device-side wait expired; the CTA gave up */
+#define MLA_DEV_TIMEOUT 0x4u   /* a bounded device-side wait expired (or the pipeline could not start); the CTA gave up */
 
 /* Supported ranges. */
 #define MLA_D_QK 576           /* query / key width: 512 latent + 64 rope */
@@ -110,7 +110,8 @@ int mla_verify_auto_nsplit(int B, int q_len, int H, int max_seq, int num_sms, si
  *   nsplit     0 = automatic (mla_verify_auto_nsplit), else 1..MLA_MAX_NSPLIT key splits
  *   workspace  device scratch of ws_bytes >= mla_verify_workspace_bytes(B,q_len,H,nsplit_used),
  *              256-byte aligned; may be NULL when the split count used is 1
- * Limits: 1 <= q_len <= 16, 1 <= H <= 128, 0 <= B <= 65535 (B == 0 is a no-op), n_pool >= 1.
+ * Limits: 1 <= q_len <= 16, 1 <= H <= 128, 0 <= B <= 65535 (B == 0 is a no-op),
+ *         1 <= n_pool <= 2^31 - 1, B * q_len * H <= 2^31 - 1.
  */
 int mla_verify_attn(const void* q, const void* kv_cache, int64_t n_pool,
                     const int32_t* slot_table, int slot_stride, const int32_t* seq_lens,

@@ -152,7 +152,8 @@ int check_verify_args(const void* q, const void* kv, int64_t n_pool, const int32
     if (nsplit < 0 || nsplit > MLA_MAX_NSPLIT) return MLA_ERR_NSPLIT;
     if (B == 0) return MLA_OK;
     if (!q || !kv || !slot || !seq_lens || !out || !lse) return MLA_ERR_NULL;
-    if (n_pool < 1 || slot_stride < q_len) return MLA_ERR_SHAPE;
+    if (n_pool < 1 || n_pool > 0x7fffffffLL || slot_stride < q_len) return MLA_ERR_SHAPE;
+    if ((long long)B * q_len * H > 0x7fffffffLL) return MLA_ERR_SHAPE;
     if (!isfinite(scale)) return MLA_ERR_ARG;
     if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(slot, 4) ||
         !aligned(seq_lens, 4) || !aligned(lse, 4))
@@ -215,8 +216,12 @@ int mla_verify_auto_nsplit(int B, int q_len, int H, int max_seq, int num_sms, si
     if (B <= 0 || q_len < 1 || H < 1 || max_seq < 1 || num_sms < 1) return 1;
     const long long tiles = ((long long)q_len * H + PLAN_ROWS_PER_CTA - 1) / PLAN_ROWS_PER_CTA;
     const long long ctas = (long long)B * tiles;
-    const long long target = (long long)num_sms * PLAN_CTAS_PER_SM;
-    long long ns = (target + ctas - 1) / ctas;
+    // one full wave of CTAs (rounded down, so no CTA spills into a second wave); with
+    // several streams of unequal lengths, two waves let the block scheduler even out
+    // the per-stream imbalance
+    const long long waves = B > 1 ? 2 : 1;
+    const long long target = (long long)num_sms * PLAN_CTAS_PER_SM * waves;
+    long long ns = target / ctas;
     const long long by_len = (max_seq + PLAN_MIN_KEYS_PER_SPLIT - 1) / PLAN_MIN_KEYS_PER_SPLIT;
     if (ns > by_len) ns = by_len;
     if (ns > MLA_MAX_NSPLIT) ns = MLA_MAX_NSPLIT;

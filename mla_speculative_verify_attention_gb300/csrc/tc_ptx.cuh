@@ -56,6 +56,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// -------------------------------------------------------------------- TMA
+// 2-D tiled load of the tensor map's box at (x = column, y = row) into shared memory;
+// completion is counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -73,6 +87,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
+}
+// Arrive on `bar` once all cp.async issued so far by this thread have landed; the arrival
+// counts toward the barrier's expected count (no increment first).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // -------------------------------------------------------------------- TMEM
@@ -134,6 +153,15 @@ __device__ __forceinline__ void tmem_st_wait() {
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Same with the 128-byte swizzle (layout type 2): rows of 128 B whose 16-byte chunks are
+// XOR-permuted by (row % 8), 8-row atoms of 1024 B.  K-major: SBO = atom stride along
+// M/N, LBO unused (the 16-element K step stays inside a 128-byte row; advance the start
+// address by 32 B per step).  M/N-major: LBO = stride between 64-element M/N chunks,
+// SBO = stride between 8-row K groups.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return smem_desc(addr, lbo, sbo) | (2ull << 61);
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator:

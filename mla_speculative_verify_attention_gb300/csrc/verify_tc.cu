@@ -2,28 +2,35 @@
 //
 // One CTA handles up to 96 query rows (r = t * H + h of one stream) over one key
 // split.  Per tile of 32 keys:
-//   S   = Q K^T        tcgen05.mma M=128 (query rows) x N=32 (keys) x K=576, fp32 in TMEM
-//   P   = softmax(S)   one thread per query row reads its S row from TMEM, applies
-//                      the draft mask, keeps a running max / sum (online softmax)
-//                      and writes P (bf16) to shared memory
-//   O^T += V^T P^T     tcgen05.mma M=128 (value dims) x N=rows x K=32 (keys), four
-//                      128-dim chunks, fp32 accumulators resident in TMEM
-// Computing P V transposed keeps O^T in 4 x rows <= 384 TMEM columns, so the
-// two S buffers (64 columns) fit beside it in the 512-column TMEM and Q K^T is
-// computed once per tile.  The same shared-memory key tile is the K-major B
-// operand of Q K^T and the M-major A operand of V^T P^T (V = first 512 dims).
+//   gather   four warps copy the tile's 32 key rows (slot-table indexed, 576 bf16
+//            each) with 16-byte cp.async into a 128-byte-swizzled shared-memory
+//            stage; arrivals are asynchronous, so a warp moves on to the next tile
+//            while its copies are in flight (measured on GB300: random 1152-byte
+//            rows gather about twice as fast this way as with TMA tile::gather4,
+//            whose per-instruction cost caps a 512-byte gather)
+//   S        = Q K^T: tcgen05.mma M=128 (query rows) x N=32 (keys) x K=576, fp32 in TMEM
+//   P        = softmax(S): one thread per query row reads its S row from TMEM, applies
+//            the draft mask, keeps a running max / sum (online softmax) and writes
+//            P (bf16) to shared memory
+//   O^T     += V^T P^T: tcgen05.mma M=128 (value dims) x N=rows x K=32 (keys), four
+//            128-dim chunks, fp32 accumulators resident in TMEM
+// Computing P V transposed keeps O^T in 4 x rows <= 384 TMEM columns, so two S
+// buffers (64 columns) fit beside it in the 512-column TMEM and Q K^T runs once
+// per tile.  The same swizzled key stage is the K-major B operand of Q K^T and the
+// M-major A operand of V^T P^T (V = first 512 dims of each key row).
 //
-// Warp roles (256 threads):
+// Warp roles (320 threads):
 //   warp 0      TMEM allocation; lane 0 issues every MMA and commit
-//   warps 1-3   slot-table gather of key tiles into a 3-stage ring (warp w owns
-//               stage w-1), 16-byte cp.async through the page_size=1 slot table
-//   warps 4-7   softmax (thread = query row = TMEM lane) and the epilogue
-//               (thread = value dim = TMEM lane of O^T)
-// The head-tile amortisation, warp-per-key dot products and NSPLIT tuning of
-// "The Occupancy Epiphany" pages are replaced here by packing heads x drafts as
-// MMA rows and by the split-count policy of the host code.
+//   warp 1      TMA copies of the Q tile (nine 64-dim boxes of R rows)
+//   warps 2-5   softmax (thread = query row = TMEM lane) and the epilogue
+//               (thread = value dim = TMEM lane of O^T); TMEM lane quadrant = warp % 4
+//   warps 6-9   key-tile gather into a 3-stage ring; warp 6 + w copies keys 8w .. 8w+7
+// The pages' sm_120 designs (head-tile amortisation, warp-per-key dot products,
+// NSPLIT tuning) are replaced by packing heads x drafts as MMA rows, a slot-table
+// gather sized to the SM's load path, and the split-count policy of the host code.
 #include "internal.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace mla {
 namespace {
@@ -33,17 +40,17 @@ using namespace tc;
 constexpr int NK = 32;                               // keys per tile
 constexpr int STAGES = 3;                            // key-tile ring
 constexpr int MAX_R = 96;                            // query rows per CTA
-constexpr int NTHREADS = 256;
-constexpr int DB = D_QK / 8;                         // 72 blocks of 8 dims
-constexpr int KB_BYTES = DB * 128;                   // one 8-key block of a tile: 9216 B
-constexpr int STAGE_BYTES = (NK / 8) * KB_BYTES;     // 36864 B
+constexpr int NTHREADS = 320;
+constexpr int GATHER_WARPS = 4;
+constexpr int NCHUNK = D_QK / 64;                    // 9 swizzled 64-dim regions per row
+constexpr int REGION = NK * 128;                     // one 64-dim region of a stage: 4096 B
+constexpr int STAGE_BYTES = NCHUNK * REGION;         // 36864 B
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int O_COL0 = 2 * NK;                       // O^T columns start after two S buffers
 constexpr float TAU = 8.0f;                          // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
-// barrier indices
 enum { B_KV_FULL = 0, B_KV_EMPTY = 3, B_S_FULL = 6, B_S_FREE = 8, B_P_FULL = 10, B_Q_FULL = 11, N_BARS = 12 };
 
 struct Layout {
@@ -52,14 +59,15 @@ struct Layout {
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
+// Q: nine regions of R rows x 128 B (MMA rows R..127 read on into the next region and,
+// past the last one, into the key stages: those rows' scores are never used).
 __host__ __device__ inline Layout layout_for(int R) {
     Layout L;
     L.q_off = 0;
-    const int q_bytes = DB * R * 16 + (128 - R) * 16;      // rows R..127 read past the end: a zero tail
-    L.kv_off = align_up(q_bytes, 1024);
+    L.kv_off = align_up(NCHUNK * R * 128, 1024);
     L.p_off = L.kv_off + STAGES * STAGE_BYTES;
     L.misc_off = align_up(L.p_off + R * NK * 2, 128);
-    L.total = L.misc_off + 128 + 128 + 512 + 512;         // barriers, tmem slot / flags, alpha[], 1/l[]
+    L.total = L.misc_off + 128 + 128 + 512 + 512;     // barriers, tmem slot / flags, alpha[], 1/l[]
     return L;
 }
 
@@ -85,13 +93,13 @@ __device__ __forceinline__ void give_up(const Misc& m, unsigned* status) {
     if (atomicExch(const_cast<int*>(m.abort), 1) == 0) atomicOr(status, DEV_TIMEOUT);
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1) verify_tc_kernel(const VerifyArgs a, int R, int R_step) {
+__global__ void __launch_bounds__(NTHREADS, 1)
+    verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap q_map, int R, int R_step) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const Layout L = layout_for(R);
     const Misc M = misc_at(smem, L);
-    uint8_t* q_s = smem + L.q_off;
     uint8_t* p_s = smem + L.p_off;
-    const uint32_t q_addr = smem_u32(q_s), kv_addr = smem_u32(smem + L.kv_off), p_addr = smem_u32(p_s);
+    const uint32_t q_addr = smem_u32(smem + L.q_off), kv_addr = smem_u32(smem + L.kv_off), p_addr = smem_u32(p_s);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -102,7 +110,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) verify_tc_kernel(const VerifyArgs
     const bool bad_len = n < a.q_len || n > a.slot_stride;
     int k_begin = 0, k_end = 0;
     if (!bad_len) split_range(n, a.nsplit, s, NK, &k_begin, &k_end);
-    const int T = (k_end - k_begin + NK - 1) / NK;
+    // the swizzled layouts need a 1024-byte aligned base: otherwise report and do no work
+    const bool misaligned = (smem_u32(smem) & 1023u) != 0;
+    const int T = misaligned ? 0 : (k_end - k_begin + NK - 1) / NK;
     const int p = n - a.q_len;
 
     // ---- set-up: TMEM, barriers
@@ -111,8 +121,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) verify_tc_kernel(const VerifyArgs
         tmem_relinquish();
     }
     if (tid == 32) {
-        for (int i = 0; i < 3; ++i) {
-            mbar_init(&M.bars[B_KV_FULL + i], 32);
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&M.bars[B_KV_FULL + i], 32 * GATHER_WARPS);
             mbar_init(&M.bars[B_KV_EMPTY + i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -120,56 +130,45 @@ __global__ void __launch_bounds__(NTHREADS, 1) verify_tc_kernel(const VerifyArgs
             mbar_init(&M.bars[B_S_FREE + i], 128);
         }
         mbar_init(&M.bars[B_P_FULL], 128);
-        mbar_init(&M.bars[B_Q_FULL], 160);
-        *M.abort = 0;
+        mbar_init(&M.bars[B_Q_FULL], 1);
+        *M.abort = misaligned ? 1 : 0;
         mbar_init_fence();
         if (bad_len) atomicOr(a.status, DEV_BAD_LEN);
+        if (misaligned) atomicOr(a.status, DEV_TIMEOUT);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *M.tmem_slot;
 
-    // ---- queries of this CTA's rows -> Q tile (A operand, K-major, no swizzle):
-    //      row r, dims 8 db .. 8 db + 7 at db * (R * 16) + r * 16; rows >= nrows and
-    //      the tail read by MMA rows R..127 are zero.
-    if (warp == 0 || warp >= 4) {
-        const int qt = warp == 0 ? lane : tid - 96;          // 0..159
-        const __nv_bfloat16* qsrc = a.q + ((int64_t)b * rows + row0) * D_QK;
-        for (int idx = qt; idx < DB * R; idx += 160) {
-            const int db = idx / R, r = idx % R;
-            const uint32_t dst = q_addr + db * (R * 16) + r * 16;
-            if (r < nrows) cp_async16(dst, qsrc + (int64_t)r * D_QK + db * 8);
-            else *reinterpret_cast<uint4*>(q_s + db * (R * 16) + r * 16) = make_uint4(0, 0, 0, 0);
-        }
-        for (int i = qt; i < 128 - R; i += 160)
-            *reinterpret_cast<uint4*>(q_s + DB * R * 16 + i * 16) = make_uint4(0, 0, 0, 0);
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        mbar_arrive(&M.bars[B_Q_FULL]);
-    }
-
     if (warp == 0) {
         // ================= MMA issuer =================
         if (lane == 0 && T > 0) {
             const uint32_t id_qk = idesc_bf16(128, NK, false, false);
             const uint32_t id_pv = idesc_bf16(128, R, true, false);
+            // Q: K-major, 128-byte swizzle, 8-row groups 1024 B apart; a 16-dim step moves 32 B
+            // inside the 128-byte rows, a 64-dim step moves to the next region (R * 128 B)
+            const uint64_t dq = smem_desc_sw128(q_addr, 16, 1024);
+            // key stage: the same layout with 32-row regions (REGION bytes)
+            const uint64_t dk = smem_desc_sw128(kv_addr, 16, 1024);
+            // V^T: M-major, 64-dim chunks REGION apart, 8-key groups 1024 B apart
+            const uint64_t dv = smem_desc_sw128(kv_addr, REGION, 1024);
+            // P: K-major, no swizzle, 8-key blocks R * 16 B apart, 8-row blocks 128 B apart
+            const uint64_t dp = smem_desc(p_addr, R * 16, 128);
+            const uint32_t q_region16 = (uint32_t)(R * 128) >> 4;
             bool ok = mbar_wait(&M.bars[B_Q_FULL], 0, M.abort);
             auto issue_pv = [&](int j) {
                 ok = ok && mbar_wait(&M.bars[B_P_FULL], j & 1, M.abort);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t st = kv_addr + (j % STAGES) * STAGE_BYTES;
+                const uint64_t st16 = (uint64_t)((j % STAGES) * STAGE_BYTES) >> 4;
 #pragma unroll
                 for (int ci = 0; ci < 4; ++ci)
 #pragma unroll
-                    for (int kk = 0; kk < NK / 16; ++kk) {
-                        // A = V^T (M = 128 dims, K = 16 keys), M-major: dim blocks 128 B apart, key blocks KB_BYTES apart
-                        const uint64_t ad = smem_desc(st + ci * 16 * 128 + kk * 2 * KB_BYTES, KB_BYTES, 128);
-                        // B = P (N = R rows, K = 16 keys), K-major: key blocks R*16 apart, row blocks 128 B apart
-                        const uint64_t bd = smem_desc(p_addr + kk * 2 * (R * 16), R * 16, 128);
-                        mma_bf16(tmem + O_COL0 + ci * R, ad, bd, id_pv, j > 0 || kk > 0);
-                    }
+                    for (int kk = 0; kk < NK / 16; ++kk)
+                        mma_bf16(tmem + O_COL0 + ci * R,
+                                 dv + st16 + (uint64_t)((2 * ci * REGION + kk * 2048) >> 4),
+                                 dp + (uint64_t)((kk * 2 * R * 16) >> 4), id_pv, j > 0 || kk > 0);
                 mma_commit(&M.bars[B_KV_EMPTY + j % STAGES]);
             };
             for (int i = 0; i < T && ok; ++i) {
@@ -177,15 +176,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) verify_tc_kernel(const VerifyArgs
                 ok = mbar_wait(&M.bars[B_KV_FULL + st], (i / STAGES) & 1, M.abort);
                 if (ok && i >= 2) ok = mbar_wait(&M.bars[B_S_FREE + (i & 1)], ((i - 2) >> 1) & 1, M.abort);
                 if (!ok) break;
+                fence_proxy_async_smem();              // cp.async (generic proxy) data -> tensor-core reads
                 tc_fence_after();
-                const uint32_t kv_st = kv_addr + st * STAGE_BYTES;
-#pragma unroll 4
+                const uint64_t st16 = (uint64_t)(st * STAGE_BYTES) >> 4;
+                const uint32_t d_s = tmem + (i & 1) * NK;
+#pragma unroll
                 for (int ks = 0; ks < D_QK / 16; ++ks) {
-                    // A = Q (M = 128 rows, K = 16 dims): dim blocks R*16 apart, row blocks 128 B apart
-                    const uint64_t ad = smem_desc(q_addr + ks * 2 * (R * 16), R * 16, 128);
-                    // B = K tile (N = 32 keys, K = 16 dims): dim blocks 128 B apart, key blocks KB_BYTES apart
-                    const uint64_t bd = smem_desc(kv_st + ks * 2 * 128, 128, KB_BYTES);
-                    mma_bf16(tmem + (i & 1) * NK, ad, bd, id_qk, ks > 0);
+                    const uint32_t qo = (uint32_t)(ks >> 2) * q_region16 + (uint32_t)(ks & 3) * 2;
+                    const uint32_t ko = (uint32_t)(((ks >> 2) * REGION + (ks & 3) * 32) >> 4);
+                    mma_bf16(d_s, dq + qo, dk + st16 + ko, id_qk, ks > 0);
                 }
                 mma_commit(&M.bars[B_S_FULL + (i & 1)]);
                 if (i >= 1) issue_pv(i - 1);
@@ -194,44 +193,53 @@ __global__ void __launch_bounds__(NTHREADS, 1) verify_tc_kernel(const VerifyArgs
             if (!ok) give_up(M, a.status);
         }
         __syncwarp();
-    } else if (warp <= 3) {
-        // ================= key-tile gather =================
-        const int st = warp - 1;
+    } else if (warp == 1) {
+        // ================= Q tile copies =================
+        if (T > 0 && lane == 0) {
+            mbar_arrive_expect_tx(&M.bars[B_Q_FULL], (uint32_t)(NCHUNK * R * 128));
+            const int qrow = b * rows + row0;
+#pragma unroll
+            for (int c = 0; c < NCHUNK; ++c)
+                tma_load_2d(q_addr + c * R * 128, &q_map, c * 64, qrow, &M.bars[B_Q_FULL]);
+        }
+    } else if (warp >= 6) {
+        // ================= key-tile gather: keys 8w .. 8w+7 of every tile =================
+        const int w = warp - 6;
         bool bad_slot = false;
-        const uint32_t dst0 = kv_addr + st * STAGE_BYTES + (lane & 7) * 16;
-        for (int i = st; i < T; i += STAGES) {
+        const int32_t* slot_row = a.slot + (int64_t)b * a.slot_stride;
+        // lane l copies 16-byte pieces f = l, l + 32, ... of the warp's 8 rows x 72 pieces;
+        // consecutive lanes take consecutive pieces of a row (contiguous global reads)
+        for (int i = 0; i < T; ++i) {
+            const int st = i % STAGES;
+            int sl = 0;
+            if (lane < 8) {
+                const int j = min(k_begin + i * NK + 8 * w + lane, k_end - 1);   // past the split: repeat a valid key
+                sl = slot_row[j];
+                if (sl < 0 || (int64_t)sl >= a.n_pool) { bad_slot = true; sl = 0; }
+            }
             if (i >= STAGES && !mbar_wait(&M.bars[B_KV_EMPTY + st], ((i - STAGES) / STAGES) & 1, M.abort)) {
                 give_up(M, a.status);
                 break;
             }
-            const int k0 = k_begin + i * NK;
-            int64_t slot[NK / 8];
+            const uint32_t base = kv_addr + st * STAGE_BYTES;
 #pragma unroll
-            for (int gk = 0; gk < NK / 8; ++gk) {
-                const int j = min(k0 + gk * 8 + (lane & 7), k_end - 1);   // past the split: repeat a valid key
-                int64_t sl = a.slot[(int64_t)b * a.slot_stride + j];
-                if (sl < 0 || sl >= a.n_pool) { bad_slot = true; sl = 0; }
-                slot[gk] = sl;
+            for (int it = 0; it < 8 * (D_QK / 8) / 32; ++it) {          // 18 pieces per lane
+                const int f = it * 32 + lane;
+                const int rr = f / (D_QK / 8), pc = f % (D_QK / 8);
+                const int key = 8 * w + rr;
+                const int row_slot = __shfl_sync(0xffffffffu, sl, rr);
+                const uint32_t dst = base + (pc >> 3) * REGION + key * 128 + (((pc & 7) ^ (key & 7)) << 4);
+                cp_async16(dst, a.kv + (int64_t)row_slot * D_QK + pc * 8);
             }
-#pragma unroll
-            for (int gk = 0; gk < NK / 8; ++gk) {
-                const __nv_bfloat16* src = a.kv + slot[gk] * D_QK;
-#pragma unroll 6
-                for (int it = 0; it < DB / 4; ++it) {
-                    const int pc = it * 4 + (lane >> 3);           // 16-byte piece = dim block
-                    cp_async16(dst0 + gk * KB_BYTES + pc * 128, src + pc * 8);
-                }
-            }
-            cp_async_wait_all();
-            fence_proxy_async_smem();
-            mbar_arrive(&M.bars[B_KV_FULL + st]);
+            cp_async_arrive_noinc(&M.bars[B_KV_FULL + st]);
         }
+        cp_async_wait_all();
         if (bad_slot) atomicOr(a.status, DEV_BAD_SLOT);
     } else {
         // ================= softmax + epilogue =================
-        const int sw = warp - 4;                       // TMEM lane quadrant
-        const int r = sw * 32 + lane;                  // query row of this thread (S lane)
-        const uint32_t lane_base = (uint32_t)(sw * 32) << 16;
+        const int quad = warp & 3;                     // TMEM lane quadrant of this warp
+        const int r = quad * 32 + lane;                // query row of this thread (S lane)
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const bool row_ok = r < nrows;
         const int t = row_ok ? (row0 + r) / a.H : 0;
         unsigned vis = 0;
@@ -241,6 +249,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) verify_tc_kernel(const VerifyArgs
                 vis |= (seen ? 1u : 0u) << d;
             }
         const float c2 = a.scale * LOG2E;
+        const int plain_end = min(p, k_end);           // keys below this need no mask
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int i = 0; i < T; ++i) {
@@ -256,12 +265,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) verify_tc_kernel(const VerifyArgs
             const int k0 = k_begin + i * NK;
             float x[NK];
             float mt = -INFINITY;
+            if (k0 + NK <= plain_end) {                // the whole tile is prefix keys of this split
 #pragma unroll
-            for (int k = 0; k < NK; ++k) {
-                const int j = k0 + k;
-                const bool vk = row_ok && j < k_end && (j < p || ((vis >> (j - p)) & 1u));
-                x[k] = vk ? __uint_as_float(sv[k]) * c2 : -INFINITY;
-                mt = fmaxf(mt, x[k]);
+                for (int k = 0; k < NK; ++k) {
+                    x[k] = row_ok ? __uint_as_float(sv[k]) * c2 : -INFINITY;
+                    mt = fmaxf(mt, x[k]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < NK; ++k) {
+                    const int j = k0 + k;
+                    const bool vk = row_ok && j < k_end && (j < p || ((vis >> (j - p)) & 1u));
+                    x[k] = vk ? __uint_as_float(sv[k]) * c2 : -INFINITY;
+                    mt = fmaxf(mt, x[k]);
+                }
             }
             const bool need = mt > m + TAU;
             float alpha = 1.f;
@@ -302,7 +319,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) verify_tc_kernel(const VerifyArgs
             }
             l += ladd;
             if (r < R) {
-                // P (B operand, K-major): keys 8 kb .. 8 kb + 7 of row r at kb * (R * 16) + r * 16
+                // P (B operand, K-major, no swizzle): keys 8 kb .. 8 kb + 7 of row r at kb * (R * 16) + r * 16
 #pragma unroll
                 for (int kb = 0; kb < NK / 8; ++kb)
                     *reinterpret_cast<uint4*>(p_s + kb * (R * 16) + r * 16) =
@@ -322,16 +339,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) verify_tc_kernel(const VerifyArgs
         else if (l > 0.f) { inv = 1.f / l; lse_v = (m + log2f(l)) * LN2; }
         else { inv = 0.f; lse_v = -INFINITY; }
         M.rinv[r] = inv;
-        const int64_t grow = (int64_t)b * rows + row0 + r;
+        const int64_t grow0 = (int64_t)b * rows + row0;
         if (row_ok) {
-            if (a.nsplit == 1) a.lse[grow] = lse_v;
-            else a.part_lse[grow * a.nsplit + s] = lse_v;
+            if (a.nsplit == 1) a.lse[grow0 + r] = lse_v;
+            else a.part_lse[(grow0 + r) * a.nsplit + s] = lse_v;
         }
         bar_sync(2, 128);
+        // O^T -> rows: thread = TMEM lane = value dim, each warp store writes 32 consecutive
+        // dims (128 B) of one row
         const bool have_o = T > 0 && !failed;
-        const int64_t grow0 = (int64_t)b * rows + row0;
         for (int ci = 0; ci < 4; ++ci) {
-            const int dim = ci * 128 + sw * 32 + lane;
+            const int dim = ci * 128 + quad * 32 + lane;
             for (int c0 = 0; c0 < nrows; c0 += 16) {
                 uint32_t v[16];
                 if (have_o) {
@@ -385,11 +403,14 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
     }
     int n_tiles, R_step, R;
     tc_tiling(a.q_len * a.H, &n_tiles, &R_step, &R);
+    CUtensorMap q_map;
+    const uint64_t q_rows = (uint64_t)a.B * a.q_len * a.H;
+    if (!encode_bf16_2d_sw128(&q_map, a.q, D_QK, q_rows, D_QK * 2, 64, (uint32_t)R,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+        return cudaErrorInvalidValue;
     dim3 grid(a.nsplit, n_tiles, a.B);
-    verify_tc_kernel<<<grid, NTHREADS, layout_for(R).total, stream>>>(a, R, R_step);
+    verify_tc_kernel<<<grid, NTHREADS, layout_for(R).total, stream>>>(a, q_map, R, R_step);
     return cudaGetLastError();
 }
-
-int tc_smem_bytes(int R) { return layout_for(R).total; }
 
 }  // namespace mla

@@ -1,7 +1,10 @@
-"""Pins the tensor-core descriptor conventions the verify kernel relies on: a
-128 x N x K bf16 product through tcgen05.mma with operands in the canonical
-no-swizzle shared-memory layouts (A K-major and A M-major, B K-major), read back
-from TMEM, against a float64 matmul of the same bf16 values."""
+"""Pins the tensor-core and TMA conventions the verify kernel relies on.
+
+* tcgen05.mma 128 x N x K bf16 products with operands in the canonical shared-memory
+  layouts -- no swizzle and 128-byte swizzle, A K-major and M-major, B K-major --
+  read back from TMEM, against a float64 matmul of the same bf16 values;
+* a TMA 2-D tile load (box 64 x R, 128-byte swizzle): the exact shared-memory bytes
+  against the swizzled arrangement computed here."""
 import ctypes
 import os
 import subprocess
@@ -23,13 +26,15 @@ def probe():
     subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-std=c++17", "-shared",
                     "-Xcompiler", "-fPIC", "-o", lib, src], check=True)
     L = ctypes.CDLL(lib)
-    P = ctypes.c_void_p
-    L.umma_probe.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
-    L.umma_probe.restype = ctypes.c_int
+    P, I = ctypes.c_void_p, ctypes.c_int
+    L.umma_probe.argtypes = [P, P, P, I, I, I, I, I, I, P, P]
+    L.umma_probe.restype = I
+    L.tma_tile_probe.argtypes = [P, ctypes.c_longlong, I, I, P, P, P]
+    L.tma_tile_probe.restype = I
     return L
 
 
-def _run(L, N, K, a_mode, swap, seed=0):
+def _gemm(L, N, K, a_mode, a_sw, b_sw, swap=0, seed=0):
     rng = np.random.default_rng(seed)
     a = torch.from_numpy(rng.normal(size=(128, K)).astype(np.float32)).to(torch.bfloat16)
     b = torch.from_numpy(rng.normal(size=(N, K)).astype(np.float32)).to(torch.bfloat16)
@@ -37,7 +42,7 @@ def _run(L, N, K, a_mode, swap, seed=0):
     ad, bd = a.cuda().contiguous(), b.cuda().contiguous()
     d = torch.full((128, N), float("nan"), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = L.umma_probe(ad.data_ptr(), bd.data_ptr(), d.data_ptr(), N, K, a_mode, swap, st.data_ptr(),
+    rc = L.umma_probe(ad.data_ptr(), bd.data_ptr(), d.data_ptr(), N, K, a_mode, a_sw, b_sw, swap, st.data_ptr(),
                       torch.cuda.current_stream().cuda_stream)
     assert rc == 0
     torch.cuda.synchronize()
@@ -47,12 +52,53 @@ def _run(L, N, K, a_mode, swap, seed=0):
 
 @pytest.mark.parametrize("N", [32, 80, 96])
 def test_k_major_a(probe, N):
-    err = _run(probe, N, 64, 0, 0)
-    assert err < 1e-3, err
+    assert _gemm(probe, N, 64, 0, 0, 0) < 1e-3
 
 
 @pytest.mark.parametrize("N", [32, 80, 96])
 def test_m_major_a(probe, N):
-    e_plain = _run(probe, N, 32, 1, 0)
-    e_swap = _run(probe, N, 32, 1, 1)
+    e_plain = _gemm(probe, N, 32, 1, 0, 0)
+    e_swap = _gemm(probe, N, 32, 1, 0, 0, swap=1)
     assert e_plain < 1e-3, f"M-major A with LBO along K / SBO along M: err {e_plain}; swapped fields: err {e_swap}"
+
+
+@pytest.mark.parametrize("N", [32, 64, 96])
+def test_sw128_k_major_a_and_b(probe, N):
+    assert _gemm(probe, N, 64, 0, 1, 1) < 1e-3
+    assert _gemm(probe, N, 64, 0, 1, 0) < 1e-3
+
+
+@pytest.mark.parametrize("N", [32, 80, 96])
+def test_sw128_m_major_a(probe, N):
+    e_plain = _gemm(probe, N, 32, 1, 1, 0)
+    e_swap = _gemm(probe, N, 32, 1, 1, 0, swap=1)
+    assert e_plain < 1e-3, f"SW128 M-major A, LBO = M-chunk stride / SBO = K-group stride: {e_plain}; swapped: {e_swap}"
+
+
+def _expected_sw128(src_rows: np.ndarray, rows_per_region: int) -> np.ndarray:
+    """Bytes of 9 regions (64 columns each) of rows x 128 B, chunk j of row r at (j ^ (r % 8))."""
+    R = src_rows.shape[0]
+    out = np.zeros(9 * rows_per_region * 128, dtype=np.uint8)
+    b = src_rows.view(np.uint8).reshape(R, 9, 8, 16)     # row, region, chunk, bytes
+    for r in range(R):
+        for c in range(9):
+            for j in range(8):
+                o = c * rows_per_region * 128 + r * 128 + ((j ^ (r % 8)) * 16)
+                out[o:o + 16] = b[r, c, j]
+    return out
+
+
+@pytest.mark.parametrize("R", [80, 96])
+def test_tma_tile_rows_into_sw128(probe, R):
+    rng = np.random.default_rng(4)
+    n = 700
+    src = rng.integers(0, 1 << 16, size=(n, 576), dtype=np.uint16)
+    row0 = 300
+    d_src = torch.from_numpy(src.view(np.int16)).cuda()
+    out = torch.zeros(9 * R * 128, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert probe.tma_tile_probe(d_src.data_ptr(), n, row0, R, out.data_ptr(), st.data_ptr(),
+                                torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(out.cpu().numpy(), _expected_sw128(src[row0:row0 + R], R))

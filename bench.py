@@ -118,6 +118,27 @@ def traffic_from_profiles(config: str):
 
 
 # --------------------------------------------------------------------------
+# replicas: aggregation over ranks (no collective in the data path)
+# --------------------------------------------------------------------------
+def max_over_ranks(values, device=None):
+    """Element-wise max of a list of floats over the default process group (identity
+    when torch.distributed is not initialised).  Works with gloo (CPU) and nccl."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def aggregate_throughput(bytes_per_rank: float, ms_per_step_max: float, world: int) -> float:
+    """Whole-job GB/s of N replicas that each process `bytes_per_rank` per step, timed by
+    the slowest rank."""
+    return world * bytes_per_rank / (ms_per_step_max * 1e-3) / 1e9
+
+
+# --------------------------------------------------------------------------
 # clocks sampler
 # --------------------------------------------------------------------------
 class Clocks:
@@ -362,12 +383,9 @@ def run_gpu(args):
     mean_step = statistics.mean(step_ms)
     mean_kern = statistics.mean(kern_ms)
     mean_e2e = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([mean_step, mean_kern, mean_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_step, mean_kern, mean_e2e = [float(x) for x in t.tolist()]
-    value = world * work["kv_bytes"] / (mean_step * 1e-3) / 1e9
-    e2e_value = world * work["kv_bytes"] / (mean_e2e * 1e-3) / 1e9
+    mean_step, mean_kern, mean_e2e = max_over_ranks([mean_step, mean_kern, mean_e2e], device=dev)
+    value = aggregate_throughput(work["kv_bytes"], mean_step, world)
+    e2e_value = aggregate_throughput(work["kv_bytes"], mean_e2e, world)
 
     if bound == "tensor":
         achieved = work["flops"] / (mean_kern * 1e-3) / 1e12

@@ -1,0 +1,50 @@
+"""Multi-process (gloo, world size 2, CPU) coverage of the benchmark's replica path:
+every rank runs its own copy of the workload (no exchange in the data path), the
+timing is the maximum over ranks and the throughput is summed over replicas."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    vals = bench.max_over_ranks([1.0 + rank, 5.0 - rank, 0.25 * (rank + 1)])
+    gbs = bench.aggregate_throughput(1e9, vals[0], world)
+    q.put((rank, vals, gbs))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_aggregate_with_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    for rank, vals, gbs in out:
+        assert vals == [2.0, 5.0, 0.5]                 # max over the two ranks
+        assert gbs == pytest.approx(2 * 1e9 / 2e-3 / 1e9)   # two replicas, slowest rank's 2 ms
+
+
+def test_single_process_is_identity():
+    import bench
+    assert bench.max_over_ranks([3.0, 4.0]) == [3.0, 4.0]
+    assert bench.aggregate_throughput(2e9, 1.0, 1) == pytest.approx(2000.0)

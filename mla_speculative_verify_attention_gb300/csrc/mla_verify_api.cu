@@ -47,81 +47,78 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // ---------------------------------------------------------------------------
-// Combine: one CTA of 128 threads per (row, 32 output dims).  Thread (sg, dv)
-// with sg = tid / 8, dv = tid % 8 accumulates the float4 dv of the chunk over
-// splits s = sg, sg + 16, ...; the 16 partial sums are added in shared memory.
+// Combine: one CTA of 256 threads per (row, 128 output dims).  Warp 0 turns the
+// row's S split log-sum-exps into the row's lse and the split weights
+// w_s = exp(lse_s - lse) (in shared memory); then thread (g, v), g = tid / 32,
+// v = tid % 32, sums float4 v of the 128 dims over splits s = g, g + 8, ... (many
+// independent 16-byte loads in flight), and the 8 group sums are added in shared
+// memory.  The launch may overlap the tail of the split kernel before it
+// (programmatic dependent launch); griddepcontrol.wait holds every thread until
+// that kernel has completed and its writes are visible.
 // ---------------------------------------------------------------------------
-constexpr int CB_THREADS = 128;
-constexpr int CB_DIMS = 32;
-
-__device__ __forceinline__ float block_max128(float v, float* red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    v = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    __syncthreads();
-    return v;
-}
-__device__ __forceinline__ float block_sum128(float v, float* red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    v = (red[0] + red[1]) + (red[2] + red[3]);
-    __syncthreads();
-    return v;
-}
+constexpr int CB_THREADS = 256;
+constexpr int CB_DIMS = 128;
+constexpr int CB_GROUPS = CB_THREADS / 32;
 
 __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __restrict__ part_out,
                                                              const float* __restrict__ part_lse, int S,
                                                              float* __restrict__ out, float* __restrict__ lse) {
-    __shared__ float red[4];
-    __shared__ float4 acc_s[16][8];
-    const int tid = threadIdx.x;
-    const int chunk = blockIdx.y;
+    extern __shared__ float wsm[];                  // [S] split weights
+    __shared__ float4 acc_s[CB_GROUPS][32];
+    __shared__ float row_stat[2];                   // lse, state (0 ok, 1 empty, 2 malformed)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int tid = threadIdx.x, lane = tid & 31, g = tid >> 5;
     const long long row = blockIdx.x;
+    const int quarter = blockIdx.y;
     const float* pl = part_lse + row * S;
 
-    float mx = -INFINITY, bad = 0.f;
-    for (int s = tid; s < S; s += CB_THREADS) {
-        float v = pl[s];
-        if (v != v) bad = 1.f;
-        mx = fmaxf(mx, v);
+    if (g == 0) {
+        float mx = -INFINITY;
+        bool bad = false;
+        for (int s = lane; s < S; s += 32) {
+            const float v = pl[s];
+            bad |= v != v;
+            mx = fmaxf(mx, v);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        bad = __any_sync(0xffffffffu, bad);
+        float z = 0.f;
+        if (!bad && mx != -INFINITY)
+            for (int s = lane; s < S; s += 32) z += expf(pl[s] - mx);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        const float L = mx + logf(z);
+        for (int s = lane; s < S; s += 32) wsm[s] = (bad || mx == -INFINITY) ? 0.f : expf(pl[s] - L);
+        if (lane == 0) {
+            row_stat[0] = bad ? __int_as_float(0x7fc00000) : (mx == -INFINITY ? -INFINITY : L);
+            row_stat[1] = bad ? 2.f : (mx == -INFINITY ? 1.f : 0.f);
+        }
     }
-    mx = block_max128(mx, red);
-    bad = block_max128(bad, red);
-    float* o = out + row * D_V + chunk * CB_DIMS;
-    if (bad != 0.f || mx == -INFINITY) {          // malformed stream or no visible key
-        if (tid < 8) reinterpret_cast<float4*>(o)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (chunk == 0 && tid == 0) lse[row] = bad != 0.f ? __int_as_float(0x7fc00000) : -INFINITY;
-        return;
-    }
-    float z = 0.f;
-    for (int s = tid; s < S; s += CB_THREADS) z += expf(pl[s] - mx);
-    z = block_sum128(z, red);
-    const float L = mx + logf(z);
-
-    const int sg = tid >> 3, dv = tid & 7;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = sg; s < S; s += 16) {
-        float w = expf(pl[s] - L);
-        if (w == 0.f) continue;
-        float4 v = reinterpret_cast<const float4*>(part_out + (row * S + s) * D_V + chunk * CB_DIMS)[dv];
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-    }
-    acc_s[sg][dv] = acc;
     __syncthreads();
-    if (tid < 8) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row_stat[1] == 0.f) {
+        const float* base = part_out + row * (long long)S * D_V + quarter * CB_DIMS + lane * 4;
+#pragma unroll 4
+        for (int s = g; s < S; s += CB_GROUPS) {
+            const float w = wsm[s];
+            if (w == 0.f) continue;
+            const float4 v = *reinterpret_cast<const float4*>(base + (long long)s * D_V);
+            acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+        }
+    }
+    acc_s[g][lane] = acc;
+    __syncthreads();
+    if (g == 0) {
         float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
-            float4 v = acc_s[g][tid];
+        for (int k = 0; k < CB_GROUPS; ++k) {
+            const float4 v = acc_s[k][lane];
             r.x += v.x; r.y += v.y; r.z += v.z; r.w += v.w;
         }
-        reinterpret_cast<float4*>(o)[tid] = r;
+        reinterpret_cast<float4*>(out + row * D_V + quarter * CB_DIMS)[lane] = r;
+        if (quarter == 0 && lane == 0) lse[row] = row_stat[0];
     }
-    if (chunk == 0 && tid == 0) lse[row] = L;
 }
 
 }  // namespace
@@ -129,9 +126,17 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __rest
 cudaError_t launch_combine(const float* part_out, const float* part_lse, long long n_rows, int S,
                            float* out, float* lse, cudaStream_t stream) {
     if (n_rows <= 0) return cudaSuccess;
-    dim3 grid((unsigned)n_rows, D_V / CB_DIMS);
-    combine_kernel<<<grid, CB_THREADS, 0, stream>>>(part_out, part_lse, S, out, lse);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n_rows, D_V / CB_DIMS);
+    cfg.blockDim = dim3(CB_THREADS);
+    cfg.dynamicSmemBytes = (size_t)S * sizeof(float);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, part_out, part_lse, S, out, lse);
 }
 
 }  // namespace mla

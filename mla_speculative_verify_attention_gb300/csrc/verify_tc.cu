@@ -372,9 +372,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     }
 
-    // ---- teardown
+    // ---- teardown; the combine launched after this kernel may now be scheduled
     tc_fence_before();
     __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);

@@ -147,6 +147,39 @@ int mla_verify_combine(const float* part_out, const float* part_lse, int B, int 
                        int S, float* out, float* lse, mla_stream_t stream);
 
 /*
+ * fp8 sparse decode ("The Occupancy Probe", section "The Scene: What Came Before":
+ * DeepSeek-V4's decode attention over scattered fp8 KV cache gathers with per-token
+ * scales and top-k token lists): q_len = 1, every head of stream b attends to the
+ * topk keys listed in topk_slots[b], with no mask:
+ *     k_j = [ decode_e4m3(kv_lat[s_j, 0:512]) * kv_scale[s_j] | kv_rope[s_j, 0:64] ]
+ *     v_j = decode_e4m3(kv_lat[s_j, 0:512]) * kv_scale[s_j]
+ *     out[b,h] = softmax_j(scale * q[b,h] . k_j) v_j,  lse[b,h] = ln sum_j exp(...)
+ * decode_e4m3 is the OCP FP8 E4M3 ("fn") value of the byte.  The kernel converts
+ * codes to bf16 exactly and applies kv_scale to the latent scores and to the
+ * softmax weights, so the dequantisation adds no rounding.
+ *   q          bf16 [B, H, 576] (= [B, 1, H, 576]), 16-byte aligned
+ *   kv_lat     uint8 [n_pool, 512] e4m3 codes, 16-byte aligned
+ *   kv_scale   fp32 [n_pool]
+ *   kv_rope    bf16 [n_pool, 64], 16-byte aligned
+ *   topk_slots int32 [B, topk], pool rows (any order; duplicates count twice)
+ *   out fp32 [B, H, 512], lse fp32 [B, H]; nsplit / workspace as for mla_verify_attn
+ *   (mla_verify_workspace_bytes(B, 1, H, nsplit)).
+ * Limits: 1 <= H <= 128, 0 <= B <= 65535, topk >= 1, 1 <= n_pool <= 2^31 - 1.
+ * An index outside [0, n_pool) sets MLA_DEV_BAD_SLOT and reads pool row 0.
+ */
+int mla_sparse_fp8_decode(const void* q, const uint8_t* kv_lat_e4m3, const float* kv_scale, const void* kv_rope,
+                          int64_t n_pool, const int32_t* topk_slots, int topk, int B, int H, float scale,
+                          float* out, float* lse, int nsplit, void* workspace, size_t ws_bytes,
+                          mla_stream_t stream);
+
+/* The split stage of mla_sparse_fp8_decode() alone (nsplit >= 1 explicit), like
+ * mla_verify_partials(); partials then merge with mla_verify_combine(..., q_len = 1, ...). */
+int mla_sparse_fp8_partials(const void* q, const uint8_t* kv_lat_e4m3, const float* kv_scale, const void* kv_rope,
+                            int64_t n_pool, const int32_t* topk_slots, int topk, int B, int H, float scale,
+                            float* out, float* lse, int nsplit, void* workspace, size_t ws_bytes,
+                            mla_stream_t stream);
+
+/*
  * Verify attention without a caller-provided workspace, for callers that cannot
  * allocate device memory: plugins hosted by a runtime that owns all device
  * memory (a serving engine's caching allocator or a fixed arena that must not

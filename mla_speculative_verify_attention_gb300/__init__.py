@@ -32,7 +32,8 @@ DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = ("mla_verify_workspace_bytes", "mla_verify_auto_nsplit", "mla_verify_attn",
            "mla_verify_partials", "mla_verify_combine", "mla_verify_status",
-           "mla_status_string", "mla_verify_version", "mla_verify_attn_static_scratch")
+           "mla_status_string", "mla_verify_version", "mla_verify_attn_static_scratch",
+           "mla_sparse_fp8_decode", "mla_sparse_fp8_partials")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
@@ -66,6 +67,10 @@ def load():
     sig = [P, P, I64, P, I, P, P, I, I, I, F, P, P, I, P, SZ, P]
     for fn in ("mla_verify_attn", "mla_verify_partials"):
         getattr(L, fn).argtypes = sig
+        getattr(L, fn).restype = I
+    fsig = [P, P, P, P, I64, P, I, I, I, F, P, P, I, P, SZ, P]
+    for fn in ("mla_sparse_fp8_decode", "mla_sparse_fp8_partials"):
+        getattr(L, fn).argtypes = fsig
         getattr(L, fn).restype = I
     L.mla_verify_attn_static_scratch.argtypes = [P, P, I64, P, I, P, P, I, I, I, F, P, P, I, P]
     L.mla_verify_attn_static_scratch.restype = I
@@ -166,6 +171,47 @@ def verify_attn_static_scratch(q: torch.Tensor, kv_cache: torch.Tensor, slot_tab
                                           slot_table.shape[1], _ptr(seq_lens), _ptr(draft_mask), B, q_len, H,
                                           float(scale), _ptr(out), _ptr(lse), nsplit, _stream(stream))
     _check("mla_verify_attn_static_scratch", rc)
+    return out, lse
+
+
+def _check_fp8_tensors(q, kv_lat, kv_scale, kv_rope, topk_slots):
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[-1] != D_QK:
+        raise ValueError("q must be bfloat16 [B, H, 576]")
+    if kv_lat.dtype != torch.uint8 or kv_lat.dim() != 2 or kv_lat.shape[1] != D_V:
+        raise ValueError("kv_lat must be uint8 [n_pool, 512] (e4m3 codes)")
+    if kv_scale.dtype != torch.float32 or kv_scale.shape != (kv_lat.shape[0],):
+        raise ValueError("kv_scale must be float32 [n_pool]")
+    if kv_rope.dtype != torch.bfloat16 or kv_rope.shape != (kv_lat.shape[0], 64):
+        raise ValueError("kv_rope must be bfloat16 [n_pool, 64]")
+    if topk_slots.dtype != torch.int32 or topk_slots.dim() != 2:
+        raise ValueError("topk_slots must be int32 [B, topk]")
+    for t in (q, kv_lat, kv_scale, kv_rope, topk_slots):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+
+
+def sparse_fp8_decode(q, kv_lat, kv_scale, kv_rope, topk_slots, scale, *, out=None, lse=None, nsplit: int = 0,
+                      workspace=None, stream=None, partials_only: bool = False):
+    """mla_sparse_fp8_decode (or, with partials_only, mla_sparse_fp8_partials, which then
+    returns the workspace views): out [B, H, 512], lse [B, H] fp32."""
+    L = load()
+    _check_fp8_tensors(q, kv_lat, kv_scale, kv_rope, topk_slots)
+    B, H, _ = q.shape
+    topk = topk_slots.shape[1]
+    if out is None:
+        out = torch.empty((B, H, D_V), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        ns = nsplit if nsplit > 0 else auto_nsplit(B, 1, H, topk, num_sms(q.device), 1 << 62)
+        workspace = torch.empty(max(workspace_bytes(B, 1, H, ns), 256), dtype=torch.uint8, device=q.device)
+    fn = "mla_sparse_fp8_partials" if partials_only else "mla_sparse_fp8_decode"
+    rc = getattr(L, fn)(_ptr(q), _ptr(kv_lat), _ptr(kv_scale), _ptr(kv_rope), kv_lat.shape[0], _ptr(topk_slots),
+                        topk, B, H, float(scale), _ptr(out), _ptr(lse), nsplit, _ptr(workspace), workspace.numel(),
+                        _stream(stream))
+    _check(fn, rc)
+    if partials_only and nsplit > 1:
+        return workspace_views(workspace, B, 1, H, nsplit)
     return out, lse
 
 

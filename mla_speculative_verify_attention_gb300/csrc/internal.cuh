@@ -33,6 +33,14 @@ struct VerifyArgs {
     float* part_lse;              // [B, q_len, H, nsplit]
     int nsplit;
     unsigned* status;             // device status word
+    // fp8 sparse decode (kv_fp8 != 0): keys come from per-stream index lists
+    // (slot = topk_slots [B, slot_stride = topk], seq_lens unused, q_len = 1) and
+    // each key row is an e4m3 latent [512] with a per-token fp32 scale plus a bf16
+    // rope [64]; kv is unused.
+    int kv_fp8;
+    const uint8_t* kv_lat;
+    const float* kv_scale;
+    const __nv_bfloat16* kv_rope;
 };
 
 // Key range [begin, end) of split s of a stream with n keys: S contiguous

@@ -207,9 +207,71 @@ int run_verify(bool combine, const void* q, const void* kv, int64_t n_pool, cons
     return MLA_OK;
 }
 
+int run_sparse_fp8(bool combine, const void* q, const uint8_t* kv_lat, const float* kv_scale, const void* kv_rope,
+                   int64_t n_pool, const int32_t* topk_slots, int topk, int B, int H, float scale, float* out,
+                   float* lse, int nsplit, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (B < 0 || B > 65535 || H < 1 || H > MLA_MAX_HEADS) return MLA_ERR_SHAPE;
+    if (nsplit < 0 || nsplit > MLA_MAX_NSPLIT) return MLA_ERR_NSPLIT;
+    if (!combine && nsplit == 0) return MLA_ERR_NSPLIT;
+    if (B == 0) return MLA_OK;
+    if (!q || !kv_lat || !kv_scale || !kv_rope || !topk_slots || !out || !lse) return MLA_ERR_NULL;
+    if (topk < 1 || n_pool < 1 || n_pool > 0x7fffffffLL || (long long)B * H > 0x7fffffffLL) return MLA_ERR_SHAPE;
+    if (!isfinite(scale)) return MLA_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(kv_lat, 16) || !aligned(kv_rope, 16) || !aligned(kv_scale, 4) ||
+        !aligned(topk_slots, 4) || !aligned(out, 16) || !aligned(lse, 4))
+        return MLA_ERR_ALIGN;
+    unsigned* status = nullptr;
+    int num_sms = 0;
+    int rc = device_state(nullptr, &status, &num_sms);
+    if (rc != MLA_OK) return rc;
+    int ns = nsplit > 0 ? nsplit : mla_verify_auto_nsplit(B, 1, H, topk, num_sms, ws ? ws_bytes : 0);
+    const long long rows = (long long)B * H;
+    VerifyArgs a;
+    memset(&a, 0, sizeof a);
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.n_pool = n_pool;
+    a.slot = topk_slots;
+    a.slot_stride = topk;
+    a.B = B; a.q_len = 1; a.H = H;
+    a.scale = scale;
+    a.out = out; a.lse = lse;
+    a.nsplit = ns;
+    a.status = status;
+    a.kv_fp8 = 1;
+    a.kv_lat = kv_lat;
+    a.kv_scale = kv_scale;
+    a.kv_rope = static_cast<const __nv_bfloat16*>(kv_rope);
+    if (ns > 1) {
+        size_t need = mla_verify_workspace_bytes(B, 1, H, ns);
+        if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+        if (!aligned(ws, 256)) return MLA_ERR_ALIGN;
+        a.part_out = static_cast<float*>(ws);
+        a.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)rows * ns * D_V * 4));
+    }
+    if (launch_verify_tc(a, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+    if (combine && ns > 1 && launch_combine(a.part_out, a.part_lse, rows, ns, out, lse, stream) != cudaSuccess)
+        return MLA_ERR_LAUNCH;
+    return MLA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int mla_sparse_fp8_decode(const void* q, const uint8_t* kv_lat_e4m3, const float* kv_scale, const void* kv_rope,
+                          int64_t n_pool, const int32_t* topk_slots, int topk, int B, int H, float scale, float* out,
+                          float* lse, int nsplit, void* workspace, size_t ws_bytes, mla_stream_t stream) {
+    return run_sparse_fp8(true, q, kv_lat_e4m3, kv_scale, kv_rope, n_pool, topk_slots, topk, B, H, scale, out, lse,
+                          nsplit, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_sparse_fp8_partials(const void* q, const uint8_t* kv_lat_e4m3, const float* kv_scale, const void* kv_rope,
+                            int64_t n_pool, const int32_t* topk_slots, int topk, int B, int H, float scale,
+                            float* out, float* lse, int nsplit, void* workspace, size_t ws_bytes,
+                            mla_stream_t stream) {
+    return run_sparse_fp8(false, q, kv_lat_e4m3, kv_scale, kv_rope, n_pool, topk_slots, topk, B, H, scale, out, lse,
+                          nsplit, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
 
 size_t mla_verify_workspace_bytes(int B, int q_len, int H, int nsplit) {
     if (B < 0 || q_len < 1 || H < 1 || nsplit < 1 || nsplit == 1) return 0;

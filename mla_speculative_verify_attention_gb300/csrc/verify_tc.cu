@@ -28,6 +28,8 @@
 // The pages' sm_120 designs (head-tile amortisation, warp-per-key dot products,
 // NSPLIT tuning) are replaced by packing heads x drafts as MMA rows, a slot-table
 // gather sized to the SM's load path, and the split-count policy of the host code.
+#include <cuda_fp8.h>
+
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -46,7 +48,10 @@ constexpr int NCHUNK = D_QK / 64;                    // 9 swizzled 64-dim region
 constexpr int REGION = NK * 128;                     // one 64-dim region of a stage: 4096 B
 constexpr int STAGE_BYTES = NCHUNK * REGION;         // 36864 B
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int O_COL0 = 2 * NK;                       // O^T columns start after two S buffers
+// TMEM columns: S buffers first (bf16 path: two of 32 columns; fp8 path: two pairs
+// of latent / rope scores), then O^T
+template <bool FP8> constexpr int s_cols() { return FP8 ? 2 * NK : NK; }
+template <bool FP8> constexpr int o_col0() { return 2 * s_cols<FP8>(); }
 constexpr float TAU = 8.0f;                          // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -67,7 +72,8 @@ __host__ __device__ inline Layout layout_for(int R) {
     L.kv_off = align_up(NCHUNK * R * 128, 1024);
     L.p_off = L.kv_off + STAGES * STAGE_BYTES;
     L.misc_off = align_up(L.p_off + R * NK * 2, 128);
-    L.total = L.misc_off + 128 + 128 + 512 + 512;     // barriers, tmem slot / flags, alpha[], 1/l[]
+    L.total = L.misc_off + 128 + 128 + 512 + 512 + STAGES * NK * 4;  // barriers, tmem slot / flags,
+                                                                     // alpha[], 1/l[], fp8 key scales
     return L;
 }
 
@@ -77,6 +83,7 @@ struct Misc {
     volatile int* abort;
     float* alpha;
     float* rinv;
+    float* kscale;                // [STAGES][NK] per-key scales of the fp8 path
 };
 
 __device__ __forceinline__ Misc misc_at(uint8_t* smem, const Layout& L) {
@@ -86,6 +93,7 @@ __device__ __forceinline__ Misc misc_at(uint8_t* smem, const Layout& L) {
     m.abort = reinterpret_cast<volatile int*>(smem + L.misc_off + 132);
     m.alpha = reinterpret_cast<float*>(smem + L.misc_off + 256);
     m.rinv = reinterpret_cast<float*>(smem + L.misc_off + 768);
+    m.kscale = reinterpret_cast<float*>(smem + L.misc_off + 1280);
     return m;
 }
 
@@ -93,8 +101,31 @@ __device__ __forceinline__ void give_up(const Misc& m, unsigned* status) {
     if (atomicExch(const_cast<int*>(m.abort), 1) == 0) atomicOr(status, DEV_TIMEOUT);
 }
 
+// Sixteen e4m3 codes -> sixteen bf16 values (exact: every e4m3 value is a bf16 value),
+// packed as two 16-byte groups of eight.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4& raw, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+            const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)(w[i] >> (16 * hlf));
+            const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3));
+            const float2 f = __half22float2(h);
+            const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+            o[2 * i + hlf] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+template <bool FP8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap q_map, int R, int R_step) {
+    constexpr int SC = s_cols<FP8>();
+    constexpr int O_COL0 = o_col0<FP8>();
     extern __shared__ __align__(1024) uint8_t smem[];
     const Layout L = layout_for(R);
     const Misc M = misc_at(smem, L);
@@ -106,14 +137,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int rows = a.q_len * a.H;
     const int row0 = g * R_step;
     const int nrows = min(R_step, rows - row0);
-    const int n = a.seq_lens[b];
-    const bool bad_len = n < a.q_len || n > a.slot_stride;
+    const int n = FP8 ? a.slot_stride : a.seq_lens[b];
+    const bool bad_len = FP8 ? false : (n < a.q_len || n > a.slot_stride);
     int k_begin = 0, k_end = 0;
     if (!bad_len) split_range(n, a.nsplit, s, NK, &k_begin, &k_end);
     // the swizzled layouts need a 1024-byte aligned base: otherwise report and do no work
     const bool misaligned = (smem_u32(smem) & 1023u) != 0;
     const int T = misaligned ? 0 : (k_end - k_begin + NK - 1) / NK;
-    const int p = n - a.q_len;
+    const int p = FP8 ? n : n - a.q_len;                 // first draft key (none on the fp8 path)
 
     // ---- set-up: TMEM, barriers
     if (warp == 0) {
@@ -179,12 +210,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 fence_proxy_async_smem();              // cp.async (generic proxy) data -> tensor-core reads
                 tc_fence_after();
                 const uint64_t st16 = (uint64_t)(st * STAGE_BYTES) >> 4;
-                const uint32_t d_s = tmem + (i & 1) * NK;
+                const uint32_t d_s = tmem + (i & 1) * SC;
 #pragma unroll
                 for (int ks = 0; ks < D_QK / 16; ++ks) {
                     const uint32_t qo = (uint32_t)(ks >> 2) * q_region16 + (uint32_t)(ks & 3) * 2;
                     const uint32_t ko = (uint32_t)(((ks >> 2) * REGION + (ks & 3) * 32) >> 4);
-                    mma_bf16(d_s, dq + qo, dk + st16 + ko, id_qk, ks > 0);
+                    // fp8 path: latent dims (ks < 32) and rope dims accumulate separately, so
+                    // the per-key scale can multiply the latent part alone
+                    const bool rope = FP8 && ks >= D_V / 16;
+                    mma_bf16(rope ? d_s + NK : d_s, dq + qo, dk + st16 + ko, id_qk,
+                             rope ? ks > D_V / 16 : ks > 0);
                 }
                 mma_commit(&M.bars[B_S_FULL + (i & 1)]);
                 if (i >= 1) issue_pv(i - 1);
@@ -207,8 +242,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int w = warp - 6;
         bool bad_slot = false;
         const int32_t* slot_row = a.slot + (int64_t)b * a.slot_stride;
-        // lane l copies 16-byte pieces f = l, l + 32, ... of the warp's 8 rows x 72 pieces;
-        // consecutive lanes take consecutive pieces of a row (contiguous global reads)
+        // bf16 path: lane l copies 16-byte pieces f = l, l + 32, ... of the warp's 8 rows x
+        // 72 pieces; consecutive lanes take consecutive pieces of a row (contiguous reads)
         for (int i = 0; i < T; ++i) {
             const int st = i % STAGES;
             int sl = 0;
@@ -222,16 +257,54 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 break;
             }
             const uint32_t base = kv_addr + st * STAGE_BYTES;
+            if constexpr (!FP8) {
 #pragma unroll
-            for (int it = 0; it < 8 * (D_QK / 8) / 32; ++it) {          // 18 pieces per lane
-                const int f = it * 32 + lane;
-                const int rr = f / (D_QK / 8), pc = f % (D_QK / 8);
-                const int key = 8 * w + rr;
-                const int row_slot = __shfl_sync(0xffffffffu, sl, rr);
-                const uint32_t dst = base + (pc >> 3) * REGION + key * 128 + (((pc & 7) ^ (key & 7)) << 4);
-                cp_async16(dst, a.kv + (int64_t)row_slot * D_QK + pc * 8);
+                for (int it = 0; it < 8 * (D_QK / 8) / 32; ++it) {      // 18 pieces per lane
+                    const int f = it * 32 + lane;
+                    const int rr = f / (D_QK / 8), pc = f % (D_QK / 8);
+                    const int key = 8 * w + rr;
+                    const int row_slot = __shfl_sync(0xffffffffu, sl, rr);
+                    const uint32_t dst = base + (pc >> 3) * REGION + key * 128 + (((pc & 7) ^ (key & 7)) << 4);
+                    cp_async16(dst, a.kv + (int64_t)row_slot * D_QK + pc * 8);
+                }
+                cp_async_arrive_noinc(&M.bars[B_KV_FULL + st]);
+            } else {
+                // latent: row it of the warp's 8, lane = 16 e4m3 codes (dims 16 lane .. 16 lane + 15);
+                // rope: 8 rows x 8 pieces of 16 bytes, two per lane.  All loads first, then
+                // convert and store into the same swizzled layout as the bf16 path.
+                uint4 raw[8], rope[2];
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int row_slot = __shfl_sync(0xffffffffu, sl, it);
+                    raw[it] = __ldg(reinterpret_cast<const uint4*>(a.kv_lat + (int64_t)row_slot * D_V) + lane);
+                }
+#pragma unroll
+                for (int it = 0; it < 2; ++it) {
+                    const int f = it * 32 + lane;
+                    const int row_slot = __shfl_sync(0xffffffffu, sl, f >> 3);
+                    rope[it] = __ldg(reinterpret_cast<const uint4*>(a.kv_rope + (int64_t)row_slot * 64) + (f & 7));
+                }
+                const float ksc = lane < 8 ? __ldg(a.kv_scale + sl) : 0.f;
+                if (lane < 8) M.kscale[st * NK + 8 * w + lane] = ksc;
+                uint8_t* sbase = smem + L.kv_off + st * STAGE_BYTES;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int key = 8 * w + it;
+                    uint4 lo, hi;
+                    e4m3x16_to_bf16(raw[it], lo, hi);
+                    const int region = lane >> 2, j0 = (lane & 3) * 2;
+                    *reinterpret_cast<uint4*>(sbase + region * REGION + key * 128 + ((j0 ^ (key & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4*>(sbase + region * REGION + key * 128 + (((j0 + 1) ^ (key & 7)) << 4)) = hi;
+                }
+#pragma unroll
+                for (int it = 0; it < 2; ++it) {
+                    const int f = it * 32 + lane;
+                    const int key = 8 * w + (f >> 3), c = f & 7;
+                    *reinterpret_cast<uint4*>(sbase + 8 * REGION + key * 128 + ((c ^ (key & 7)) << 4)) = rope[it];
+                }
+                fence_proxy_async_smem();              // generic stores -> tensor-core reads
+                mbar_arrive(&M.bars[B_KV_FULL + st]);
             }
-            cp_async_arrive_noinc(&M.bars[B_KV_FULL + st]);
         }
         cp_async_wait_all();
         if (bad_slot) atomicOr(a.status, DEV_BAD_SLOT);
@@ -257,8 +330,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (bar_red_or(1, 128, !ok)) { ok = false; break; }
             tc_fence_after();
             uint32_t sv[NK];
-            tmem_ld32(tmem + lane_base + (i & 1) * NK, sv);
-            tmem_ld_wait();
+            tmem_ld32(tmem + lane_base + (i & 1) * SC, sv);
+            float ksc[FP8 ? NK : 1];
+            if constexpr (FP8) {
+                // s = scale * (scale_t * q_lat . k8 + q_rope . k_rope)
+                uint32_t sr[NK];
+                tmem_ld32(tmem + lane_base + (i & 1) * SC + NK, sr);
+                tmem_ld_wait();
+                // the key scales were written before the tile's kv_full arrival
+                ok = mbar_wait(&M.bars[B_KV_FULL + i % STAGES], (i / STAGES) & 1, M.abort);
+#pragma unroll
+                for (int k = 0; k < NK; ++k) {
+                    ksc[k] = M.kscale[(i % STAGES) * NK + k];
+                    sv[k] = __float_as_uint(ksc[k] * __uint_as_float(sv[k]) + __uint_as_float(sr[k]));
+                }
+            } else {
+                tmem_ld_wait();
+            }
             tc_fence_before();
             mbar_arrive(&M.bars[B_S_FREE + (i & 1)]);
 
@@ -288,7 +376,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 m = mt;
             }
             const bool any = bar_red_or(1, 128, need);
-            if (i >= 1) ok = mbar_wait(&M.bars[B_KV_EMPTY + (i - 1) % STAGES], ((i - 1) / STAGES) & 1, M.abort);
+            if (ok && i >= 1) ok = mbar_wait(&M.bars[B_KV_EMPTY + (i - 1) % STAGES], ((i - 1) / STAGES) & 1, M.abort);
             if (bar_red_or(1, 128, !ok)) { ok = false; break; }
             if (any && i >= 1) {
                 // O^T column r (query row r) *= alpha_r; thread = TMEM lane = value dim
@@ -314,7 +402,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int k = 0; k < NK; k += 2) {
                 const float p0 = exp2f(x[k] - mu), p1 = exp2f(x[k + 1] - mu);
                 ladd += p0 + p1;                        // the row sum keeps fp32 probabilities
-                __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+                // fp8 path: V = scale_t * e4m3 code, so P V = (P scale_t) code
+                const float f0 = FP8 ? p0 * ksc[k] : p0, f1 = FP8 ? p1 * ksc[FP8 ? k + 1 : 0] : p1;
+                __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
                 pk[k / 2] = *reinterpret_cast<uint32_t*>(&h);
             }
             l += ladd;
@@ -397,8 +487,11 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(verify_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  layout_for(MAX_R).total);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(verify_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     layout_for(MAX_R).total);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -410,7 +503,8 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
                               CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
         return cudaErrorInvalidValue;
     dim3 grid(a.nsplit, n_tiles, a.B);
-    verify_tc_kernel<<<grid, NTHREADS, layout_for(R).total, stream>>>(a, q_map, R, R_step);
+    if (a.kv_fp8) verify_tc_kernel<true><<<grid, NTHREADS, layout_for(R).total, stream>>>(a, q_map, R, R_step);
+    else verify_tc_kernel<false><<<grid, NTHREADS, layout_for(R).total, stream>>>(a, q_map, R, R_step);
     return cudaGetLastError();
 }
 

@@ -99,6 +99,23 @@ def test_partials_needs_explicit_nsplit(lib):
     assert rc == -5
 
 
+def test_fp8_argument_errors(lib):
+    P = ctypes.c_void_p
+    f = lib.mla_sparse_fp8_decode
+    f.argtypes = [P, P, P, P, ctypes.c_int64, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, P, P,
+                  ctypes.c_int, P, ctypes.c_size_t, P]
+    ok = dict(q=16, lat=16, sc=16, rope=16, n=10, ts=16, topk=4, B=2, H=8, scale=0.1, out=16, lse=16, ns=1)
+    def call(**kw):
+        a = dict(ok); a.update(kw)
+        return f(P(a["q"]), P(a["lat"]), P(a["sc"]), P(a["rope"]), a["n"], P(a["ts"]), a["topk"], a["B"], a["H"],
+                 a["scale"], P(a["out"]), P(a["lse"]), a["ns"], None, 0, None)
+    assert call(q=None) == -1 and call(lat=None) == -1 and call(ts=None) == -1
+    assert call(H=0) == -2 and call(H=129) == -2 and call(topk=0) == -2 and call(n=0) == -2
+    assert call(lat=24) == -3 and call(rope=8) == -3
+    assert call(ns=-1) == -5 and call(scale=float("nan")) == -8
+    assert call(B=0, q=None) == 0
+
+
 def test_combine_argument_errors(lib):
     P = ctypes.c_void_p
     assert lib.mla_verify_combine(None, P(16), 1, 9, 8, 4, P(16), P(16), None) == -1

@@ -47,7 +47,9 @@ WORKLOAD_TEXT = {
     "c3-16k": "MLA verify B1 q_len9 H8 prefix16384 scattered 2^20-row pool tree-mask bf16",
     "c3-64k": "MLA verify B1 q_len9 H8 prefix65536 scattered 2^20-row pool tree-mask bf16",
     "c4": "MLA verify B8 q_len9 H8 prefixes U{1024..46080} scattered 2^20-row pool tree-masks bf16",
+    "c5": "MLA fp8-e4m3 sparse decode B32 q_len1 H64 top-k 2048 of 65536 (per-token fp32 scale, bf16 rope)",
 }
+FP8_ROW_BYTES = 512 + 4 + 128          # e4m3 latent + fp32 scale + bf16 rope
 
 
 # --------------------------------------------------------------------------
@@ -76,6 +78,15 @@ def algorithmic(inp) -> dict:
     total = kv + keys * IDX_BYTES + rows * 576 * 2 + rows * (512 + 1) * 4
     return {"kv_bytes": kv, "bytes": total, "flops": flops_per_row_key() * visible_keys(inp), "keys": keys,
             "rows": rows}
+
+
+def algorithmic_fp8(f) -> dict:
+    """fp8 sparse decode: every (row, listed key) pair is visible; 644 B per key row."""
+    keys = f.B * f.topk
+    rows = f.B * f.H
+    kv = keys * FP8_ROW_BYTES
+    total = kv + keys * IDX_BYTES + rows * 576 * 2 + rows * (512 + 1) * 4
+    return {"kv_bytes": kv, "bytes": total, "flops": flops_per_row_key() * rows * f.topk, "keys": keys, "rows": rows}
 
 
 def roofline_us(work: dict, hbm_gbs: float, tflops: float) -> tuple:
@@ -190,13 +201,13 @@ class Clocks:
 # --------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # --------------------------------------------------------------------------
-def time_oracle(inp, seconds: float, max_reps: int = 1000) -> dict:
+def time_oracle(wl, seconds: float, max_reps: int = 1000) -> dict:
     import oracle
     threads = os.cpu_count() or 1
     oracle.lib()
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.verify_inputs(inp, nthreads=threads)
+        wl.oracle_call(threads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds or reps >= max_reps:
@@ -209,23 +220,27 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    inp = w.config(args.config)
-    work = algorithmic(inp)
-    steps = max(1, args.steps)
-    # each step is one full oracle call on this workload (bounded: a few seconds each)
     import oracle
+    if args.config == "c5":
+        f = w.config_fp8(args.config)
+        work = algorithmic_fp8(f)
+        call = lambda th: oracle.sparse_fp8_inputs(f, nthreads=th)
+    else:
+        inp = w.config(args.config)
+        work = algorithmic(inp)
+        call = lambda th: oracle.verify_inputs(inp, nthreads=th)
+    # each step is one full oracle call on this workload (bounded by --ref-seconds overall)
     threads = os.cpu_count() or 1
     oracle.lib()
     for _ in range(min(args.warmup, 1)):
-        oracle.verify_inputs(inp, nthreads=threads)
+        call(threads)
     times = []
-    budget = args.ref_seconds
     t_all = time.perf_counter()
-    for _ in range(steps):
+    for _ in range(max(1, args.steps)):
         t0 = time.perf_counter()
-        oracle.verify_inputs(inp, nthreads=threads)
+        call(threads)
         times.append(time.perf_counter() - t0)
-        if time.perf_counter() - t_all > budget:
+        if time.perf_counter() - t_all > args.ref_seconds:
             break
     per = statistics.mean(times)
     gbs = work["kv_bytes"] / per / 1e9
@@ -241,6 +256,105 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# --------------------------------------------------------------------------
+# workloads as seen by the GPU arm: device inputs, the split stage, the full call,
+# and the per-step host -> device inputs of the end-to-end measurement
+# --------------------------------------------------------------------------
+class VerifyWorkload:
+    def __init__(self, inp, mv, dev):
+        import torch
+        self.inp, self.mv, self.dev = inp, mv, dev
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        self.q = t(inp.q_bits.view(np.int16)).view(torch.bfloat16)
+        self.kv = t(inp.kv_bits.view(np.int16)).view(torch.bfloat16)
+        self.st, self.sl = t(inp.slot_table), t(inp.seq_lens)
+        self.mk = None if inp.mask is None else t(inp.mask)
+        self.B, self.q_len, self.H = inp.B, inp.q_len, inp.H
+        self.work = algorithmic(inp)
+        self.max_seq = inp.slot_stride
+
+    def partials(self, ns, ws, out, lse, stream):
+        return self.mv.verify_partials(self.q, self.kv, self.st, self.sl, self.mk, self.inp.scale, nsplit=ns,
+                                       workspace=ws, out=out, lse=lse, stream=stream)
+
+    def full(self, ns, ws, out, lse, stream):
+        self.mv.verify_attn(self.q, self.kv, self.st, self.sl, self.mk, self.inp.scale, out=out, lse=lse,
+                            nsplit=ns, workspace=ws, stream=stream)
+
+    def host_inputs(self):
+        """(pinned host tensor, device view to fill) pairs: queries, slot table, lengths, mask
+        and the q_len new draft KV rows of every stream (written into their pool slots)."""
+        import torch
+        inp = self.inp
+        pairs = [(torch.from_numpy(inp.q_bits.view(np.int16)).pin_memory(), self.q.view(torch.int16)),
+                 (torch.from_numpy(np.ascontiguousarray(inp.slot_table)).pin_memory(), self.st),
+                 (torch.from_numpy(np.ascontiguousarray(inp.seq_lens)).pin_memory(), self.sl)]
+        if self.mk is not None:
+            pairs.append((torch.from_numpy(np.ascontiguousarray(inp.mask)).pin_memory(), self.mk))
+        kv16 = self.kv.view(torch.int16)
+        for b in range(inp.B):
+            s = inp.slot_table[b, inp.seq_lens[b] - inp.q_len:inp.seq_lens[b]]
+            start = 0
+            for k in range(1, len(s) + 1):          # contiguous runs of draft slots: one copy each
+                if k == len(s) or s[k] != s[k - 1] + 1:
+                    rows = np.arange(s[start], s[start] + (k - start))
+                    pairs.append((torch.from_numpy(inp.kv_bits[rows].view(np.int16)).pin_memory(),
+                                  kv16[int(s[start]):int(s[start]) + (k - start)]))
+                    start = k
+        return pairs
+
+    def oracle_call(self, threads):
+        import oracle
+        oracle.verify_inputs(self.inp, nthreads=threads)
+
+
+class Fp8Workload:
+    def __init__(self, f, mv, dev):
+        import torch
+        self.f, self.mv, self.dev = f, mv, dev
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        self.q = t(f.q_bits.view(np.int16)).view(torch.bfloat16)
+        self.lat, self.sc = t(f.kv_lat), t(f.kv_scale)
+        self.rope = t(f.kv_rope.view(np.int16)).view(torch.bfloat16)
+        self.ts = t(f.topk_slots)
+        self.B, self.q_len, self.H = f.B, 1, f.H
+        self.work = algorithmic_fp8(f)
+        self.max_seq = f.topk
+
+    def partials(self, ns, ws, out, lse, stream):
+        return self.mv.sparse_fp8_decode(self.q, self.lat, self.sc, self.rope, self.ts, self.f.scale, out=out.view(self.B, self.H, 512),
+                                         lse=lse.view(self.B, self.H), nsplit=ns, workspace=ws, stream=stream,
+                                         partials_only=True)
+
+    def full(self, ns, ws, out, lse, stream):
+        self.mv.sparse_fp8_decode(self.q, self.lat, self.sc, self.rope, self.ts, self.f.scale, out=out.view(self.B, self.H, 512),
+                                  lse=lse.view(self.B, self.H), nsplit=ns, workspace=ws, stream=stream)
+
+    def host_inputs(self):
+        """Queries, top-k lists and the one new token row per stream (latent, scale, rope)."""
+        import torch
+        f = self.f
+        pairs = [(torch.from_numpy(f.q_bits.view(np.int16)).pin_memory(), self.q.view(torch.int16)),
+                 (torch.from_numpy(np.ascontiguousarray(f.topk_slots)).pin_memory(), self.ts)]
+        for b in range(f.B):
+            r = int(f.topk_slots[b, 0])
+            pairs.append((torch.from_numpy(f.kv_lat[r:r + 1].copy()).pin_memory(), self.lat[r:r + 1]))
+            pairs.append((torch.from_numpy(f.kv_scale[r:r + 1].copy()).pin_memory(), self.sc[r:r + 1]))
+            pairs.append((torch.from_numpy(f.kv_rope[r:r + 1].view(np.int16).copy()).pin_memory(),
+                          self.rope.view(torch.int16)[r:r + 1]))
+        return pairs
+
+    def oracle_call(self, threads):
+        import oracle
+        oracle.sparse_fp8_inputs(self.f, nthreads=threads)
+
+
+def make_workload(name, mv, dev):
+    if name == "c5":
+        return Fp8Workload(w.config_fp8(name), mv, dev)
+    return VerifyWorkload(w.config(name), mv, dev)
 
 
 # --------------------------------------------------------------------------
@@ -266,24 +380,15 @@ def run_gpu(args):
     import mla_speculative_verify_attention_gb300 as mv
     mv.load()
 
-    inp = w.config(args.config)
-    work = algorithmic(inp)
+    wl = make_workload(args.config, mv, dev)
+    work = wl.work
     peaks = load_peaks()
     rl_us, bound, t_mem, t_mma = roofline_us(work, peaks["hbm_gbs"], peaks["bf16_tflops"])
-
-    def dev_tensor(a, dtype=None):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return t.to(dev)
-
-    q = dev_tensor(inp.q_bits.view(np.int16)).view(torch.bfloat16)
-    kv = dev_tensor(inp.kv_bits.view(np.int16)).view(torch.bfloat16)
-    st = dev_tensor(inp.slot_table)
-    sl = dev_tensor(inp.seq_lens)
-    mk = None if inp.mask is None else dev_tensor(inp.mask)
-    ns = args.nsplit or mv.auto_nsplit(inp.B, inp.q_len, inp.H, inp.slot_stride, mv.num_sms(dev), 1 << 62)
-    ws = torch.empty(max(mv.workspace_bytes(inp.B, inp.q_len, inp.H, ns), 256), dtype=torch.uint8, device=dev)
-    out = torch.empty((inp.B, inp.q_len, inp.H, 512), dtype=torch.float32, device=dev)
-    lse = torch.empty((inp.B, inp.q_len, inp.H), dtype=torch.float32, device=dev)
+    B, q_len, H = wl.B, wl.q_len, wl.H
+    ns = args.nsplit or mv.auto_nsplit(B, q_len, H, wl.max_seq, mv.num_sms(dev), 1 << 62)
+    ws = torch.empty(max(mv.workspace_bytes(B, q_len, H, ns), 256), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, q_len, H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     launches_per_step = 1 + (1 if ns > 1 else 0)
@@ -291,16 +396,12 @@ def run_gpu(args):
     def step(e0=None, e1=None, e2=None):
         if e0 is not None:
             e0.record(stream)
+        res = wl.partials(ns, ws, out, lse, stream)
+        if e1 is not None:
+            e1.record(stream)
         if ns > 1:
-            po, pl = mv.verify_partials(q, kv, st, sl, mk, inp.scale, nsplit=ns, workspace=ws, out=out, lse=lse,
-                                        stream=stream)
-            if e1 is not None:
-                e1.record(stream)
-            mv.verify_combine(po, pl, inp.B, inp.q_len, inp.H, out=out, lse=lse, stream=stream)
-        else:
-            mv.verify_partials(q, kv, st, sl, mk, inp.scale, nsplit=1, workspace=ws, out=out, lse=lse, stream=stream)
-            if e1 is not None:
-                e1.record(stream)
+            po, pl = res
+            mv.verify_combine(po, pl, B, q_len, H, out=out, lse=lse, stream=stream)
         if e2 is not None:
             e2.record(stream)
 
@@ -327,41 +428,19 @@ def run_gpu(args):
     kern_ms = [a.elapsed_time(b) for a, b, c in ev]
     status = mv.device_status(stream)
 
-    # end to end through the C ABI with host buffers: H2D of this step's inputs
-    # (queries, slot table, lengths, mask, the q_len new draft KV rows per stream)
-    # from pinned memory, the call, and D2H of out and lse, all inside the events.
-    h_q = torch.from_numpy(inp.q_bits.view(np.int16)).pin_memory()
-    h_st = torch.from_numpy(np.ascontiguousarray(inp.slot_table)).pin_memory()
-    h_sl = torch.from_numpy(np.ascontiguousarray(inp.seq_lens)).pin_memory()
-    h_mk = None if inp.mask is None else torch.from_numpy(np.ascontiguousarray(inp.mask)).pin_memory()
-    draft_slots = [inp.slot_table[b, inp.seq_lens[b] - inp.q_len:inp.seq_lens[b]] for b in range(inp.B)]
-    h_draft = torch.from_numpy(np.concatenate([inp.kv_bits[s] for s in draft_slots]).view(np.int16)).pin_memory()
+    # end to end through the C ABI with host buffers: this step's inputs copied from
+    # pinned memory, the call (mla_verify_attn / mla_sparse_fp8_decode), and D2H of out
+    # and lse, all inside the events
+    pairs = wl.host_inputs()
     h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    q_i16 = q.view(torch.int16)
-    kv_i16 = kv.view(torch.int16)
-    draft_runs = []          # (host row offset, first pool row, count) of contiguous slot runs
-    off = 0
-    for s in draft_slots:
-        start = 0
-        for k in range(1, len(s) + 1):
-            if k == len(s) or s[k] != s[k - 1] + 1:
-                draft_runs.append((off + start, int(s[start]), k - start))
-                start = k
-        off += len(s)
-    h2d = h_q.numel() * 2 + h_st.numel() * 4 + h_sl.numel() * 4 + (0 if h_mk is None else h_mk.numel()) + \
-        h_draft.numel() * 2
+    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
     d2h = h_out.numel() * 4 + h_lse.numel() * 4
 
     def e2e_step():
-        q_i16.copy_(h_q, non_blocking=True)
-        st.copy_(h_st, non_blocking=True)
-        sl.copy_(h_sl, non_blocking=True)
-        if mk is not None:
-            mk.copy_(h_mk, non_blocking=True)
-        for ho, row, cnt in draft_runs:
-            kv_i16[row:row + cnt].copy_(h_draft[ho:ho + cnt], non_blocking=True)
-        mv.verify_attn(q, kv, st, sl, mk, inp.scale, out=out, lse=lse, nsplit=ns, workspace=ws, stream=stream)
+        for h, d in pairs:
+            d.copy_(h, non_blocking=True)
+        wl.full(ns, ws, out, lse, stream)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
@@ -396,7 +475,7 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        r = time_oracle(inp, args.cpu_seconds)
+        r = time_oracle(wl, args.cpu_seconds)
         cpu = {"value": work["kv_bytes"] / r["seconds_per_call"] / 1e9, "unit": UNIT, "cores": r["threads"],
                "kind": "oracle",
                "sample": f"{r['reps']} full fp64 oracle calls on the whole {args.config} workload "
@@ -408,8 +487,8 @@ def run_gpu(args):
         "ms_per_step": mean_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (PAGES_C2_US / (mean_step * 1e3)) if args.config == "c2" and world == 1 else None,
         "dtype": "bf16", "data": "synthetic (seeded SplitMix64 / Box-Muller inputs, shapes of the pages' workloads)",
-        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "B": inp.B, "q_len": inp.q_len,
-                   "H": inp.H, "keys": work["keys"], "n_pool": inp.n_pool, "nsplit": ns,
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "B": B, "q_len": q_len,
+                   "H": H, "keys": work["keys"], "nsplit": ns,
                    "l2": "flushed before every step (256 MiB write, outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "us_per_call": mean_step * 1e3,

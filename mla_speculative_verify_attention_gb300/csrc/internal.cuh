@@ -59,7 +59,7 @@ __host__ __device__ inline void split_range(int n, int S, int s, int tile, int* 
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
 // Row tiling of the tensor-core split kernel: n_tiles CTAs of R_step rows over
 // q_len * H rows, each padded to R (multiple of 16) MMA columns.
-void tc_tiling(int rows, int* n_tiles, int* R_step, int* R);
+void tc_tiling(int rows, int max_r, int* n_tiles, int* R_step, int* R);
 constexpr int TC_MAX_ROWS = 96;
 cudaError_t launch_combine(const float* part_out, const float* part_lse, long long n_rows, int S,
                            float* out, float* lse, cudaStream_t stream);

@@ -8,23 +8,34 @@
 //            while its copies are in flight (measured on GB300: random 1152-byte
 //            rows gather about twice as fast this way as with TMA tile::gather4,
 //            whose per-instruction cost caps a 512-byte gather)
-//   S        = Q K^T: tcgen05.mma M=128 (query rows) x N=32 (keys) x K=576, fp32 in TMEM
+//   S        = Q K^T: tcgen05.mma M=128 (query rows) x N=32 (keys) x K=576, fp32 in TMEM;
+//            the first 64-dim chunks of Q sit in TMEM (A operand read from tensor
+//            memory, no shared-memory traffic), the rest in shared memory
 //   P        = softmax(S): one thread per query row reads its S row from TMEM, applies
 //            the draft mask, keeps a running max / sum (online softmax) and writes
-//            P (bf16) to shared memory
+//            P (bf16) to one of two shared-memory buffers; it waits for P V of the
+//            previous tile only when the running max moved enough to rescale O^T, so
+//            softmax of tile i overlaps P V of tile i - 1
 //   O^T     += V^T P^T: tcgen05.mma M=128 (value dims) x N=rows x K=32 (keys), four
 //            128-dim chunks, fp32 accumulators resident in TMEM
 // Computing P V transposed keeps O^T in 4 x rows <= 384 TMEM columns, so two S
 // buffers (64 columns) fit beside it in the 512-column TMEM and Q K^T runs once
-// per tile.  The same swizzled key stage is the K-major B operand of Q K^T and the
-// M-major A operand of V^T P^T (V = first 512 dims of each key row).
+// per tile; the columns left over hold as many 32-column Q chunks as fit (4 for up
+// to 80 rows).  Measured on GB300, an M=128 x N=32 x K=16 MMA issued from a
+// converged warp takes ~17 cycles with A in TMEM and ~40 with A in shared memory
+// (bound by shared-memory reads of the 4 KB A tile), so every Q chunk moved to TMEM
+// takes four MMAs off the shared-memory port, and the freed shared memory buys a
+// fourth key stage.  The same swizzled key stage is the K-major B operand of Q K^T
+// and the M-major A operand of V^T P^T (V = first 512 dims of each key row).
 //
 // Warp roles (320 threads):
-//   warp 0      TMEM allocation; lane 0 issues every MMA and commit
-//   warp 1      TMA copies of the Q tile (nine 64-dim boxes of R rows)
-//   warps 2-5   softmax (thread = query row = TMEM lane) and the epilogue
-//               (thread = value dim = TMEM lane of O^T); TMEM lane quadrant = warp % 4
-//   warps 6-9   key-tile gather into a 3-stage ring; warp 6 + w copies keys 8w .. 8w+7
+//   warp 0      TMEM allocation; runs the MMA issue loop as a whole warp (operands
+//               stay warp-uniform) and one elected lane issues every MMA and commit
+//   warp 1      TMA copies of the shared-memory part of the Q tile (64-dim boxes of R rows)
+//   warps 2-5   Q chunks into TMEM (thread = query row), softmax (thread = query row =
+//               TMEM lane) and the epilogue (thread = value dim = TMEM lane of O^T);
+//               TMEM lane quadrant = warp % 4
+//   warps 6-9   key-tile gather into a 3- or 4-stage ring; warp 6 + w copies keys 8w .. 8w+7
 // The pages' sm_120 designs (head-tile amortisation, warp-per-key dot products,
 // NSPLIT tuning) are replaced by packing heads x drafts as MMA rows, a slot-table
 // gather sized to the SM's load path, and the split-count policy of the host code.
@@ -40,7 +51,6 @@ namespace {
 using namespace tc;
 
 constexpr int NK = 32;                               // keys per tile
-constexpr int STAGES = 3;                            // key-tile ring
 constexpr int MAX_R = 96;                            // query rows per CTA
 constexpr int NTHREADS = 320;
 constexpr int GATHER_WARPS = 4;
@@ -56,7 +66,13 @@ constexpr float TAU = 8.0f;                          // lazy rescale threshold (
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
-enum { B_KV_FULL = 0, B_KV_EMPTY = 3, B_S_FULL = 6, B_S_FREE = 8, B_P_FULL = 10, B_Q_FULL = 11, N_BARS = 12 };
+// mbarriers: key-stage full / empty per stage, then the fixed ones
+template <int STAGES> struct Bars {
+    static constexpr int KV_FULL = 0, KV_EMPTY = STAGES, S_FULL = 2 * STAGES, S_FREE = 2 * STAGES + 2,
+                         P_FULL = 2 * STAGES + 4, Q_FULL = 2 * STAGES + 6, QT_FULL = 2 * STAGES + 7,
+                         COUNT = 2 * STAGES + 8;    // P_FULL: one per P buffer
+};
+static_assert(Bars<3>::COUNT * 8 <= 128 && Bars<4>::COUNT * 8 <= 128, "barrier area");
 
 struct Layout {
     int q_off, kv_off, p_off, misc_off, total;
@@ -64,17 +80,25 @@ struct Layout {
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// Q: nine regions of R rows x 128 B (MMA rows R..127 read on into the next region and,
-// past the last one, into the key stages: those rows' scores are never used).
-__host__ __device__ inline Layout layout_for(int R) {
+// Q: the nq_s shared-memory chunks, regions of R rows x 128 B (MMA rows R..127 read on
+// into the next region and, past the last one, into the key stages: those rows' scores
+// are never used).
+__host__ __device__ inline Layout layout_for(int R, int nq_s, int stages) {
     Layout L;
     L.q_off = 0;
-    L.kv_off = align_up(NCHUNK * R * 128, 1024);
-    L.p_off = L.kv_off + STAGES * STAGE_BYTES;
-    L.misc_off = align_up(L.p_off + R * NK * 2, 128);
-    L.total = L.misc_off + 128 + 128 + 512 + 512 + STAGES * NK * 4;  // barriers, tmem slot / flags,
+    L.kv_off = align_up(nq_s * R * 128, 1024);
+    L.p_off = L.kv_off + stages * STAGE_BYTES;
+    L.misc_off = align_up(L.p_off + 2 * R * NK * 2, 128);   // two P buffers
+    L.total = L.misc_off + 128 + 128 + 512 + 512 + stages * NK * 4;  // barriers, tmem slot / flags,
                                                                      // alpha[], 1/l[], fp8 key scales
     return L;
+}
+
+// TMEM columns left for Q chunks (32 columns each) beside the S buffers and O^T.
+__host__ __device__ inline int q_tmem_chunks(bool fp8, int R) {
+    const int used = 2 * (fp8 ? 2 * NK : NK) + 4 * R;
+    const int c = ((int)TMEM_COLS - used) / 32;
+    return c < 0 ? 0 : (c > NCHUNK ? NCHUNK : c);
 }
 
 struct Misc {
@@ -83,7 +107,7 @@ struct Misc {
     volatile int* abort;
     float* alpha;
     float* rinv;
-    float* kscale;                // [STAGES][NK] per-key scales of the fp8 path
+    float* kscale;                // [stages][NK] per-key scales of the fp8 path
 };
 
 __device__ __forceinline__ Misc misc_at(uint8_t* smem, const Layout& L) {
@@ -121,13 +145,19 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4& raw, uint4& lo, uin
     hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-template <bool FP8>
+template <bool FP8, int STAGES, int NQT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap q_map, int R, int R_step) {
     constexpr int SC = s_cols<FP8>();
     constexpr int O_COL0 = o_col0<FP8>();
+    using BR = Bars<STAGES>;
+    constexpr int B_KV_FULL = BR::KV_FULL, B_KV_EMPTY = BR::KV_EMPTY, B_S_FULL = BR::S_FULL,
+                  B_S_FREE = BR::S_FREE, B_P_FULL = BR::P_FULL, B_Q_FULL = BR::Q_FULL, B_QT_FULL = BR::QT_FULL;
+    constexpr int nq_t = NQT;                            // Q chunks 0 .. NQT-1 live in TMEM,
+    constexpr int nq_s = NCHUNK - NQT;                   // chunks NQT .. 8 in shared memory
+    const int Q_COL0 = O_COL0 + 4 * R;                   // Q chunk c < nq_t: TMEM columns Q_COL0 + 32 c ..
     extern __shared__ __align__(1024) uint8_t smem[];
-    const Layout L = layout_for(R);
+    const Layout L = layout_for(R, nq_s, STAGES);
     const Misc M = misc_at(smem, L);
     uint8_t* p_s = smem + L.p_off;
     const uint32_t q_addr = smem_u32(smem + L.q_off), kv_addr = smem_u32(smem + L.kv_off), p_addr = smem_u32(p_s);
@@ -161,7 +191,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&M.bars[B_S_FREE + i], 128);
         }
         mbar_init(&M.bars[B_P_FULL], 128);
+        mbar_init(&M.bars[B_P_FULL + 1], 128);
         mbar_init(&M.bars[B_Q_FULL], 1);
+        mbar_init(&M.bars[B_QT_FULL], 128);
         *M.abort = misaligned ? 1 : 0;
         mbar_init_fence();
         if (bad_len) atomicOr(a.status, DEV_BAD_LEN);
@@ -173,12 +205,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tmem = *M.tmem_slot;
 
     if (warp == 0) {
-        // ================= MMA issuer =================
-        if (lane == 0 && T > 0) {
+        // ================= MMA issuer (lane 0) =================
+        if (T > 0) {
             const uint32_t id_qk = idesc_bf16(128, NK, false, false);
             const uint32_t id_pv = idesc_bf16(128, R, true, false);
-            // Q: K-major, 128-byte swizzle, 8-row groups 1024 B apart; a 16-dim step moves 32 B
-            // inside the 128-byte rows, a 64-dim step moves to the next region (R * 128 B)
+            // Q (shared-memory chunks): K-major, 128-byte swizzle, 8-row groups 1024 B apart;
+            // a 16-dim step moves 32 B inside the 128-byte rows, a 64-dim step moves to the
+            // next region (R * 128 B)
             const uint64_t dq = smem_desc_sw128(q_addr, 16, 1024);
             // key stage: the same layout with 32-row regions (REGION bytes)
             const uint64_t dk = smem_desc_sw128(kv_addr, 16, 1024);
@@ -188,70 +221,99 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t dp = smem_desc(p_addr, R * 16, 128);
             const uint32_t q_region16 = (uint32_t)(R * 128) >> 4;
             bool ok = mbar_wait(&M.bars[B_Q_FULL], 0, M.abort);
+            ok = ok && mbar_wait(&M.bars[B_QT_FULL], 0, M.abort);
+            ok = __all_sync(0xffffffffu, ok);
             auto issue_pv = [&](int j) {
-                ok = ok && mbar_wait(&M.bars[B_P_FULL], j & 1, M.abort);
+                ok = ok && mbar_wait(&M.bars[B_P_FULL + (j & 1)], (j >> 1) & 1, M.abort);
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) return;
                 tc_fence_after();
                 const uint64_t st16 = (uint64_t)((j % STAGES) * STAGE_BYTES) >> 4;
+                if (elect_one()) {
 #pragma unroll
                 for (int ci = 0; ci < 4; ++ci)
 #pragma unroll
                     for (int kk = 0; kk < NK / 16; ++kk)
                         mma_bf16(tmem + O_COL0 + ci * R,
                                  dv + st16 + (uint64_t)((2 * ci * REGION + kk * 2048) >> 4),
-                                 dp + (uint64_t)((kk * 2 * R * 16) >> 4), id_pv, j > 0 || kk > 0);
+                                 dp + (uint64_t)(((j & 1) * R * NK * 2 + kk * 2 * R * 16) >> 4), id_pv,
+                                 j > 0 || kk > 0);
                 mma_commit(&M.bars[B_KV_EMPTY + j % STAGES]);
+                }
+                __syncwarp();
             };
             for (int i = 0; i < T && ok; ++i) {
                 const int st = i % STAGES;
                 ok = mbar_wait(&M.bars[B_KV_FULL + st], (i / STAGES) & 1, M.abort);
                 if (ok && i >= 2) ok = mbar_wait(&M.bars[B_S_FREE + (i & 1)], ((i - 2) >> 1) & 1, M.abort);
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 fence_proxy_async_smem();              // cp.async (generic proxy) data -> tensor-core reads
                 tc_fence_after();
                 const uint64_t st16 = (uint64_t)(st * STAGE_BYTES) >> 4;
                 const uint32_t d_s = tmem + (i & 1) * SC;
+                if (elect_one()) {
 #pragma unroll
                 for (int ks = 0; ks < D_QK / 16; ++ks) {
-                    const uint32_t qo = (uint32_t)(ks >> 2) * q_region16 + (uint32_t)(ks & 3) * 2;
-                    const uint32_t ko = (uint32_t)(((ks >> 2) * REGION + (ks & 3) * 32) >> 4);
+                    const int c = ks >> 2;
+                    const uint32_t ko = (uint32_t)((c * REGION + (ks & 3) * 32) >> 4);
                     // fp8 path: latent dims (ks < 32) and rope dims accumulate separately, so
                     // the per-key scale can multiply the latent part alone
                     const bool rope = FP8 && ks >= D_V / 16;
-                    mma_bf16(rope ? d_s + NK : d_s, dq + qo, dk + st16 + ko, id_qk,
-                             rope ? ks > D_V / 16 : ks > 0);
+                    const uint32_t d = rope ? d_s + NK : d_s;
+                    const bool acc = rope ? ks > D_V / 16 : ks > 0;
+                    if (c < nq_t) {
+                        mma_bf16_ta(d, tmem + Q_COL0 + ks * 8, dk + st16 + ko, id_qk, acc);
+                    } else {
+                        const uint32_t qo = (uint32_t)(c - nq_t) * q_region16 + (uint32_t)(ks & 3) * 2;
+                        mma_bf16(d, dq + qo, dk + st16 + ko, id_qk, acc);
+                    }
                 }
                 mma_commit(&M.bars[B_S_FULL + (i & 1)]);
+                }
+                __syncwarp();
                 if (i >= 1) issue_pv(i - 1);
             }
             if (ok) issue_pv(T - 1);
-            if (!ok) give_up(M, a.status);
+            if (!ok && lane == 0) give_up(M, a.status);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ================= Q tile copies =================
         if (T > 0 && lane == 0) {
-            mbar_arrive_expect_tx(&M.bars[B_Q_FULL], (uint32_t)(NCHUNK * R * 128));
+            mbar_arrive_expect_tx(&M.bars[B_Q_FULL], (uint32_t)(nq_s * R * 128));
             const int qrow = b * rows + row0;
-#pragma unroll
-            for (int c = 0; c < NCHUNK; ++c)
-                tma_load_2d(q_addr + c * R * 128, &q_map, c * 64, qrow, &M.bars[B_Q_FULL]);
+            for (int c = nq_t; c < NCHUNK; ++c)
+                tma_load_2d(q_addr + (c - nq_t) * R * 128, &q_map, c * 64, qrow, &M.bars[B_Q_FULL]);
         }
     } else if (warp >= 6) {
         // ================= key-tile gather: keys 8w .. 8w+7 of every tile =================
         const int w = warp - 6;
         bool bad_slot = false;
         const int32_t* slot_row = a.slot + (int64_t)b * a.slot_stride;
+        // Slot indices run four tiles ahead: lane l holds the slot of key 8 w + (l & 7) of
+        // tile i0 + (l >> 3) for the current group of four tiles (cur) and the next (nxt),
+        // so a tile's row copies never wait on its own index load.  Indices are checked
+        // when their group becomes current (by then they have arrived).
+        auto load_slots = [&](int i0) -> int {
+            const int t = i0 + (lane >> 3);
+            if (t >= T) return 0;
+            const int j = min(k_begin + t * NK + 8 * w + (lane & 7), k_end - 1);   // past the split: repeat a valid key
+            return __ldg(slot_row + j);
+        };
+        int cur = load_slots(0), nxt = load_slots(4);
         // bf16 path: lane l copies 16-byte pieces f = l, l + 32, ... of the warp's 8 rows x
         // 72 pieces; consecutive lanes take consecutive pieces of a row (contiguous reads)
         for (int i = 0; i < T; ++i) {
             const int st = i % STAGES;
-            int sl = 0;
-            if (lane < 8) {
-                const int j = min(k_begin + i * NK + 8 * w + lane, k_end - 1);   // past the split: repeat a valid key
-                sl = slot_row[j];
-                if (sl < 0 || (int64_t)sl >= a.n_pool) { bad_slot = true; sl = 0; }
+            if ((i & 3) == 0) {
+                if (i > 0) {
+                    cur = nxt;
+                    nxt = load_slots(i + 4);
+                }
+                if (cur < 0 || (int64_t)cur >= a.n_pool) { bad_slot = true; cur = 0; }
             }
+            const int sl = __shfl_sync(0xffffffffu, cur, ((i & 3) << 3) + (lane & 7));   // key 8 w + (lane & 7)
             if (i >= STAGES && !mbar_wait(&M.bars[B_KV_EMPTY + st], ((i - STAGES) / STAGES) & 1, M.abort)) {
                 give_up(M, a.status);
                 break;
@@ -321,6 +383,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const bool seen = a.mask ? a.mask[((int64_t)b * a.q_len + t) * a.q_len + d] != 0 : d <= t;
                 vis |= (seen ? 1u : 0u) << d;
             }
+        if (T > 0) {
+            // Q chunks 0 .. nq_t-1 of row r into TMEM lane r (rows past the tile: zeros),
+            // two chunks (sixteen 16-byte loads) in flight at a time
+            const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * rows + row0 + r) * D_QK);
+            for (int c0 = 0; c0 < nq_t; c0 += 2) {
+                uint4 raw[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const bool have = row_ok && c0 + (j >> 3) < nq_t;
+                    raw[j] = have ? __ldg(qrow + c0 * 8 + j) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (c0 + h < nq_t) {
+                        uint32_t v[32];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            v[4 * j] = raw[8 * h + j].x; v[4 * j + 1] = raw[8 * h + j].y;
+                            v[4 * j + 2] = raw[8 * h + j].z; v[4 * j + 3] = raw[8 * h + j].w;
+                        }
+                        tmem_st32(tmem + lane_base + Q_COL0 + (c0 + h) * 32, v);
+                    }
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+        }
+        mbar_arrive(&M.bars[B_QT_FULL]);
         const float c2 = a.scale * LOG2E;
         const int plain_end = min(p, k_end);           // keys below this need no mask
         float m = -INFINITY, l = 0.f;
@@ -376,7 +466,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 m = mt;
             }
             const bool any = bar_red_or(1, 128, need);
-            if (ok && i >= 1) ok = mbar_wait(&M.bars[B_KV_EMPTY + (i - 1) % STAGES], ((i - 1) / STAGES) & 1, M.abort);
+            // P buffer i & 1 was last read by P V of tile i - 2; a rescale of O^T also needs
+            // P V of tile i - 1 complete (without one, P V of tiles i - 1 and i commute)
+            if (ok && any && i >= 1)
+                ok = mbar_wait(&M.bars[B_KV_EMPTY + (i - 1) % STAGES], ((i - 1) / STAGES) & 1, M.abort);
+            else if (ok && i >= 2)
+                ok = mbar_wait(&M.bars[B_KV_EMPTY + (i - 2) % STAGES], ((i - 2) / STAGES) & 1, M.abort);
             if (bar_red_or(1, 128, !ok)) { ok = false; break; }
             if (any && i >= 1) {
                 // O^T column r (query row r) *= alpha_r; thread = TMEM lane = value dim
@@ -412,12 +507,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // P (B operand, K-major, no swizzle): keys 8 kb .. 8 kb + 7 of row r at kb * (R * 16) + r * 16
 #pragma unroll
                 for (int kb = 0; kb < NK / 8; ++kb)
-                    *reinterpret_cast<uint4*>(p_s + kb * (R * 16) + r * 16) =
+                    *reinterpret_cast<uint4*>(p_s + (i & 1) * (R * NK * 2) + kb * (R * 16) + r * 16) =
                         make_uint4(pk[4 * kb], pk[4 * kb + 1], pk[4 * kb + 2], pk[4 * kb + 3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&M.bars[B_P_FULL]);
+            mbar_arrive(&M.bars[B_P_FULL + (i & 1)]);
         }
         if (ok && T > 0) ok = mbar_wait(&M.bars[B_KV_EMPTY + (T - 1) % STAGES], ((T - 1) / STAGES) & 1, M.abort);
         const bool failed = bar_red_or(1, 128, !ok);
@@ -474,38 +569,69 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 }  // namespace
 
-void tc_tiling(int rows, int* n_tiles, int* R_step, int* R) {
-    *n_tiles = (rows + MAX_R - 1) / MAX_R;
+void tc_tiling(int rows, int max_r, int* n_tiles, int* R_step, int* R) {
+    *n_tiles = (rows + max_r - 1) / max_r;
     *R_step = (rows + *n_tiles - 1) / *n_tiles;
     *R = (*R_step + 15) / 16 * 16;
 }
 
+namespace {
+constexpr int MAX_SMEM = 232448;                     // opt-in shared memory per block on sm_103
+
+// Instantiations: (fp8, key stages, Q chunks in TMEM).  q_tmem_chunks gives 4 for up to
+// 80 rows on the bf16 path and for up to 64 on the fp8 path, 2 beyond that (0 for fp8
+// at 96 rows); four stages fit whenever four or more chunks leave shared memory.
+template <bool FP8, int STAGES, int NQT>
+cudaError_t launch_one(bool set_attr, dim3 grid, cudaStream_t stream, const VerifyArgs& a, const CUtensorMap& q_map,
+                       int R, int R_step) {
+    auto* k = verify_tc_kernel<FP8, STAGES, NQT>;
+    if (set_attr) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SMEM);
+        if (e != cudaSuccess) return e;
+    }
+    const int smem = layout_for(R, NCHUNK - NQT, STAGES).total;
+    if (smem > MAX_SMEM) return cudaErrorInvalidConfiguration;
+    k<<<grid, NTHREADS, smem, stream>>>(a, q_map, R, R_step);
+    return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
-    static bool attr_set[64];
+    static bool attr_set[64][5];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(verify_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 layout_for(MAX_R).total);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(verify_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     layout_for(MAX_R).total);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
     int n_tiles, R_step, R;
-    tc_tiling(a.q_len * a.H, &n_tiles, &R_step, &R);
+    // fp8: at 96 rows no TMEM is left for Q and the shared-memory Q tile, three key
+    // stages and two P buffers exceed the opt-in limit, so its tiles stop at 80 rows
+    tc_tiling(a.q_len * a.H, a.kv_fp8 ? 80 : MAX_R, &n_tiles, &R_step, &R);
+    const int nq = q_tmem_chunks(a.kv_fp8, R) >= 4 ? 4 : q_tmem_chunks(a.kv_fp8, R) >= 2 ? 2 : 0;
+    const bool four = layout_for(R, NCHUNK - nq, 4).total <= MAX_SMEM;
     CUtensorMap q_map;
     const uint64_t q_rows = (uint64_t)a.B * a.q_len * a.H;
     if (!encode_bf16_2d_sw128(&q_map, a.q, D_QK, q_rows, D_QK * 2, 64, (uint32_t)R,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
         return cudaErrorInvalidValue;
     dim3 grid(a.nsplit, n_tiles, a.B);
-    if (a.kv_fp8) verify_tc_kernel<true><<<grid, NTHREADS, layout_for(R).total, stream>>>(a, q_map, R, R_step);
-    else verify_tc_kernel<false><<<grid, NTHREADS, layout_for(R).total, stream>>>(a, q_map, R, R_step);
-    return cudaGetLastError();
+    int which;
+    if (!a.kv_fp8) which = nq == 4 ? 0 : 1;
+    else which = nq == 4 ? 2 : nq == 2 ? 3 : 4;
+    const bool set = !attr_set[dev][which];
+    switch (which) {
+        case 0: e = four ? launch_one<false, 4, 4>(set, grid, stream, a, q_map, R, R_step)
+                         : cudaErrorInvalidConfiguration; break;
+        case 1: e = four ? cudaErrorInvalidConfiguration
+                         : launch_one<false, 3, 2>(set, grid, stream, a, q_map, R, R_step); break;
+        case 2: e = four ? launch_one<true, 4, 4>(set, grid, stream, a, q_map, R, R_step)
+                         : cudaErrorInvalidConfiguration; break;
+        case 3: e = four ? launch_one<true, 4, 2>(set, grid, stream, a, q_map, R, R_step)
+                         : cudaErrorInvalidConfiguration; break;
+        default: e = four ? cudaErrorInvalidConfiguration
+                          : launch_one<true, 3, 0>(set, grid, stream, a, q_map, R, R_step); break;
+    }
+    if (e == cudaSuccess) attr_set[dev][which] = true;
+    return e;
 }
 
 }  // namespace mla

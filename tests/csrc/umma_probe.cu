@@ -5,8 +5,10 @@
 //   swizzle or with the 128-byte swizzle; B K-major without or with swizzle --
 //   multiplied by tcgen05.mma into TMEM and read back with tcgen05.ld.  For the
 //   M-major A the two stride fields can be passed swapped, so one run shows which
-//   field strides along M and which along K.  Every variant reads only inside its
-//   own shared-memory region.
+//   field strides along M and which along K.  a_mode 2 puts A in TMEM instead (lane =
+//   row, two consecutive K elements per 32-bit column, written with tcgen05.st), the
+//   form used when the query tile stays in tensor memory.  Every variant reads only
+//   inside its own shared-memory region and its own TMEM columns.
 // tma_tile_probe: rows [row0, row0 + R) of a [n, 576] bf16 matrix loaded with nine
 //   2-D tile copies (box 64 columns x R rows, 128-byte swizzle) into nine regions of
 //   R x 128 B; the raw shared-memory bytes are copied out.
@@ -47,7 +49,7 @@ __global__ void __launch_bounds__(128) probe_kernel(const uint16_t* A, const uin
 
     for (int i = tid; i < (A_BYTES + B_BYTES) / 4; i += 128) reinterpret_cast<uint32_t*>(smem)[i] = 0;
     __syncthreads();
-    for (int i = tid; i < M * K; i += 128) {
+    for (int i = tid; i < M * K && a_mode != 2; i += 128) {
         int m = i / K, k = i % K;
         uint32_t off;
         if (a_mode == 0 && a_sw == 0) off = (k / 8) * 2048 + (m / 8) * 128 + (m % 8) * 16 + (k % 8) * 2;
@@ -76,6 +78,23 @@ __global__ void __launch_bounds__(128) probe_kernel(const uint16_t* A, const uin
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    constexpr uint32_t A_COL = 256;                  // A in TMEM: columns 256 .. 256 + K / 2
+    if (a_mode == 2) {
+        // thread = row m = TMEM lane (warp w reaches lanes 32 w .. 32 w + 31)
+        const int m = tid;
+        for (int c0 = 0; c0 < K / 2; c0 += 16) {
+            uint32_t r[16];
+            for (int j = 0; j < 16; ++j) {
+                const int k = 2 * (c0 + j);
+                r[j] = (uint32_t)A[m * K + k] | ((uint32_t)A[m * K + k + 1] << 16);
+            }
+            tmem_st16(tmem + ((uint32_t)(32 * warp) << 16) + A_COL + c0, r);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
 
     if (tid == 0) {
         const uint32_t idesc = idesc_bf16(M, N, a_mode == 1, false);
@@ -95,7 +114,8 @@ __global__ void __launch_bounds__(128) probe_kernel(const uint16_t* A, const uin
             }
             if (b_sw == 0) bd = smem_desc(b0 + ks * 2 * (N * 16), N * 16, 128);
             else bd = smem_desc_sw128(b0 + (ks / 4) * N * 128 + (ks % 4) * 32, 16, 1024);
-            mma_bf16(tmem, ad, bd, idesc, ks > 0);
+            if (a_mode == 2) mma_bf16_ta(tmem, tmem + A_COL + ks * 8, bd, idesc, ks > 0);
+            else mma_bf16(tmem, ad, bd, idesc, ks > 0);
         }
         mma_commit(bar);
     }
@@ -154,6 +174,7 @@ extern "C" int umma_probe(const uint16_t* A, const uint16_t* B, float* D, int N,
                           int b_sw, int swap, int* status, cudaStream_t stream) {
     if (N < 16 || N > 256 || N % 16 || K < 16 || K > 64 || K % 16) return -2;
     if (a_sw && a_mode == 0 && K != 64) return -2;
+    if (a_mode < 0 || a_mode > 2 || (a_mode == 2 && (K % 32 || a_sw))) return -2;
     if (b_sw && K != 64) return -2;
     const int smem = A_BYTES + B_BYTES + 128;
     cudaError_t e = cudaFuncSetAttribute(probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -33,7 +33,7 @@ def test_c5_full(cuda_lib):
 
 
 @pytest.mark.parametrize("nsplit", [1, 3, 0])
-@pytest.mark.parametrize("shape", [(3, 16, 77), (2, 64, 300), (1, 1, 40), (2, 128, 65), (4, 8, 1)],
+@pytest.mark.parametrize("shape", [(3, 16, 77), (2, 64, 300), (1, 1, 40), (2, 128, 65), (4, 8, 1), (2, 96, 100)],
                          ids=lambda s: f"B{s[0]}H{s[1]}k{s[2]}")
 def test_shapes(cuda_lib, shape, nsplit):
     B, H, topk = shape

@@ -1,7 +1,8 @@
 """Pins the tensor-core and TMA conventions the verify kernel relies on.
 
 * tcgen05.mma 128 x N x K bf16 products with operands in the canonical shared-memory
-  layouts -- no swizzle and 128-byte swizzle, A K-major and M-major, B K-major --
+  layouts -- no swizzle and 128-byte swizzle, A K-major and M-major, B K-major -- and
+  with A held in TMEM,
   read back from TMEM, against a float64 matmul of the same bf16 values;
 * a TMA 2-D tile load (box 64 x R, 128-byte swizzle): the exact shared-memory bytes
   against the swizzled arrangement computed here."""
@@ -53,6 +54,14 @@ def _gemm(L, N, K, a_mode, a_sw, b_sw, swap=0, seed=0):
 @pytest.mark.parametrize("N", [32, 80, 96])
 def test_k_major_a(probe, N):
     assert _gemm(probe, N, 64, 0, 0, 0) < 1e-3
+
+
+@pytest.mark.parametrize("N", [32, 64, 80, 96])
+@pytest.mark.parametrize("K", [32, 64])
+def test_tmem_a(probe, N, K):
+    """A from TMEM (lane = row, two K elements per 32-bit column, lower index low)."""
+    assert _gemm(probe, N, K, 2, 0, 0) < 1e-3
+    assert _gemm(probe, N, 64, 2, 0, 1) < 1e-3
 
 
 @pytest.mark.parametrize("N", [32, 80, 96])

@@ -8,6 +8,8 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 calls it, and it shares no code with the CUDA library.
 
 Pins (tests/test_oracle.py): brute force in high precision on tiny inputs,
+the bit-packed mask against the byte mask and a from-scratch tree closure, the
+KV append against the generator's own placement of the draft rows,
 zero-query / identical-key / single-key closed forms, split + merge identity,
 slot permutation invariance, exact score shifts, the e4m3 decode table against
 the OCP definition and torch's float8_e4m3fn, and the fp8 path against the bf16
@@ -35,6 +37,10 @@ def lib():
         L.oracle_mla_verify.argtypes = [P, P, I64, P, I32, P, P, I32, I32, I32, D, I64, I64,
                                         P, I64, P, P, I32]
         L.oracle_mla_verify.restype = I32
+        L.oracle_mla_verify_packed.argtypes = L.oracle_mla_verify.argtypes
+        L.oracle_mla_verify_packed.restype = I32
+        L.oracle_kv_append.argtypes = [P, I64, P, I32, P, P, I32, I32]
+        L.oracle_kv_append.restype = I32
         L.oracle_mla_combine.argtypes = [P, P, I64, I32, I32, P, P]
         L.oracle_mla_combine.restype = None
         L.oracle_mla_sparse_fp8.argtypes = [P, P, P, P, I64, P, I32, I32, I32, D, P, I64, P, P, I32]
@@ -72,11 +78,14 @@ def e4m3_to_f64(codes) -> np.ndarray:
 
 
 def verify(q_bits, kv_bits, slot_table, seq_lens, mask, scale, *, rows=None,
-           key_begin: int = 0, key_end: int = 2 ** 62, nthreads: Optional[int] = None):
+           key_begin: int = 0, key_end: int = 2 ** 62, nthreads: Optional[int] = None,
+           mask_bits=None):
     """Exact (fp64) MLA verify attention.
 
     q_bits [B, q_len, H, 576] uint16 (bf16 bits); kv_bits [n_pool, 576] uint16;
     slot_table [B, stride] int32; seq_lens [B] int32; mask [B, q_len, q_len] uint8 or None.
+    mask_bits [B, q_len] uint64 (bit i of word (b, t): draft t sees draft i) replaces
+    ``mask`` when given (q_len <= 64).
     Returns out [B, q_len, H, 512] and lse [B, q_len, H] (float64), or, with ``rows``
     (flat (b * q_len + t) * H + h indices), out [len(rows), 512] and lse [len(rows)].
     """
@@ -87,6 +96,9 @@ def verify(q_bits, kv_bits, slot_table, seq_lens, mask, scale, *, rows=None,
     st = _c(slot_table, np.int32)
     sl = _c(seq_lens, np.int32)
     mk = None if mask is None else _c(mask, np.uint8)
+    mb = None if mask_bits is None else _c(mask_bits, np.uint64)
+    if mb is not None:
+        assert mk is None and mb.shape == (B, q_len)
     if rows is None:
         n = B * q_len * H
         r = None
@@ -95,9 +107,10 @@ def verify(q_bits, kv_bits, slot_table, seq_lens, mask, scale, *, rows=None,
         n = r.size
     out = np.empty((n, 512), dtype=np.float64)
     lse = np.empty((n,), dtype=np.float64)
-    rc = lib().oracle_mla_verify(_ptr(q), _ptr(kv), kv.shape[0], _ptr(st), st.shape[1], _ptr(sl),
-                                 _ptr(mk), B, q_len, H, float(scale), int(key_begin), int(key_end),
-                                 _ptr(r), n, _ptr(out), _ptr(lse), nthreads or default_threads())
+    fn = lib().oracle_mla_verify if mb is None else lib().oracle_mla_verify_packed
+    rc = fn(_ptr(q), _ptr(kv), kv.shape[0], _ptr(st), st.shape[1], _ptr(sl),
+            _ptr(mk if mb is None else mb), B, q_len, H, float(scale), int(key_begin), int(key_end),
+            _ptr(r), n, _ptr(out), _ptr(lse), nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle_mla_verify failed with status {rc}")
     if rows is None:
@@ -108,6 +121,21 @@ def verify(q_bits, kv_bits, slot_table, seq_lens, mask, scale, *, rows=None,
 def verify_inputs(inp, **kw):
     """verify() on a workloads.VerifyInputs."""
     return verify(inp.q_bits, inp.kv_bits, inp.slot_table, inp.seq_lens, inp.mask, inp.scale, **kw)
+
+
+def kv_append(kv_bits, slot_table, seq_lens, new_kv_bits):
+    """KV append: a copy of kv_bits [n_pool, 576] (uint16) with row i of stream b,
+    new_kv_bits[b, i], written to pool row slot_table[b, seq_lens[b] - q_len + i]."""
+    kv = np.array(kv_bits, dtype=np.uint16, copy=True, order="C")
+    st = _c(slot_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    nk = _c(new_kv_bits, np.uint16)
+    B, q_len, D = nk.shape
+    assert D == 576 and st.shape[0] == B and sl.shape == (B,)
+    rc = lib().oracle_kv_append(_ptr(kv), kv.shape[0], _ptr(st), st.shape[1], _ptr(sl), _ptr(nk), B, q_len)
+    if rc != 0:
+        raise ValueError(f"oracle_kv_append failed with status {rc}")
+    return kv
 
 
 def combine(part_out, part_lse):

@@ -113,6 +113,7 @@ static void attend_row(const double* q, key_fn get_key, const void* ctx, int64_t
 typedef struct {
     const uint16_t* q; const uint16_t* kv; int64_t n_pool;
     const int32_t* slot; int slot_stride; const int32_t* seq_lens; const uint8_t* mask;
+    const uint64_t* mask_bits;        /* packed form of the same mask (one word per draft) */
     int B, q_len, H; double scale;
     int64_t key_begin, key_end;       /* keys j restricted to [key_begin, key_end) */
     const int64_t* rows; int64_t n_rows;
@@ -122,10 +123,12 @@ typedef struct {
 } verify_job;
 
 /* Draft t of stream b sees key j (0 <= j < n) iff j is a prefix key, or j is
- * draft i = j - p and mask[b, t, i] = 1 (NULL mask: i <= t). */
+ * draft i = j - p and mask[b, t, i] = 1 (NULL mask: i <= t).  The packed form
+ * holds the same relation as bit i of the 64-bit word mask_bits[b, t]. */
 static int visible(const verify_job* J, int b, int t, int64_t j, int64_t p) {
     if (j < p) return 1;
     int64_t i = j - p;
+    if (J->mask_bits != NULL) return (int)((J->mask_bits[(int64_t)b * J->q_len + t] >> i) & 1u);
     if (J->mask == NULL) return i <= t;
     return J->mask[((int64_t)b * J->q_len + t) * J->q_len + i] != 0;
 }
@@ -221,6 +224,64 @@ int oracle_mla_verify(const uint16_t* q, const uint16_t* kv, int64_t n_pool,
     J.key_begin = key_begin; J.key_end = key_end; J.rows = rows; J.n_rows = n_rows;
     J.out = out; J.lse = lse;
     return run_jobs(&J, nthreads, verify_worker, sizeof(verify_job));
+}
+
+/*
+ * The same with the draft mask bit-packed: bit i of mask_bits[b * q_len + t] set
+ * means draft t sees draft i (q_len <= 64); NULL means the causal chain.
+ * Larger draft trees ("The Occupancy Epiphany: How One Environment Variable
+ * Unlocked 3x Throughput ...", sections "The Broader Context" and "Input
+ * Knowledge Required": DDTree draft trees) need more than the 8-16 drafts of a
+ * chain, and one 64-bit word per draft holds a tree of up to 64 nodes.
+ */
+int oracle_mla_verify_packed(const uint16_t* q, const uint16_t* kv, int64_t n_pool,
+                             const int32_t* slot_table, int slot_stride, const int32_t* seq_lens,
+                             const uint64_t* mask_bits, int B, int q_len, int H, double scale,
+                             int64_t key_begin, int64_t key_end,
+                             const int64_t* rows, int64_t n_rows,
+                             double* out, double* lse, int nthreads) {
+    if (!q || !kv || !slot_table || !seq_lens || !out || !lse) return OR_ERR_ARG;
+    if (B < 0 || q_len < 1 || q_len > 64 || H < 1 || slot_stride < 0 || n_pool < 0) return OR_ERR_ARG;
+    verify_job J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.kv = kv; J.n_pool = n_pool; J.slot = slot_table; J.slot_stride = slot_stride;
+    J.seq_lens = seq_lens; J.mask = NULL; J.mask_bits = mask_bits; J.B = B; J.q_len = q_len; J.H = H;
+    J.scale = scale; J.key_begin = key_begin; J.key_end = key_end; J.rows = rows; J.n_rows = n_rows;
+    J.out = out; J.lse = lse;
+    return run_jobs(&J, nthreads, verify_worker, sizeof(verify_job));
+}
+
+/* ------------------------------------------------------------------------ */
+/* KV append                                                                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * Before a verify step the q_len draft rows of each stream enter the paged
+ * latent cache ("The Occupancy Epiphany: How One Environment Variable ...",
+ * section "The Broader Context": KV slots handed out by a paged allocator,
+ * possibly scattered): row i of stream b, new_kv[b, i, 0:576], is written to
+ * pool row slot_table[b, seq_lens[b] - q_len + i] (the drafts are the last
+ * q_len keys of the stream).  All lengths and slots are checked first; on an
+ * error nothing is written.
+ */
+int oracle_kv_append(uint16_t* kv, int64_t n_pool, const int32_t* slot_table, int slot_stride,
+                     const int32_t* seq_lens, const uint16_t* new_kv, int B, int q_len) {
+    if (!kv || !slot_table || !seq_lens || !new_kv || B < 0 || q_len < 1 || slot_stride < q_len) return OR_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        int64_t n = seq_lens[b];
+        if (n < q_len || n > slot_stride) return OR_ERR_LEN;
+        for (int i = 0; i < q_len; ++i) {
+            int64_t s = slot_table[(int64_t)b * slot_stride + (n - q_len + i)];
+            if (s < 0 || s >= n_pool) return OR_ERR_SLOT;
+        }
+    }
+    for (int b = 0; b < B; ++b) {
+        int64_t n = seq_lens[b];
+        for (int i = 0; i < q_len; ++i) {
+            int64_t s = slot_table[(int64_t)b * slot_stride + (n - q_len + i)];
+            memcpy(kv + s * D_QK, new_kv + ((int64_t)b * q_len + i) * D_QK, sizeof(uint16_t) * D_QK);
+        }
+    }
+    return OR_OK;
 }
 
 /* ------------------------------------------------------------------------ */

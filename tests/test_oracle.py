@@ -349,3 +349,89 @@ def test_fp8_sparse_bruteforce_tiny():
             ref = np.array([float(mpmath.fsum(ei * mpmath.mpf(float(k[d])) for ei, k in zip(e, keys)) / z)
                             for d in range(512)])
             assert np.max(np.abs(o[b, h] - ref)) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# bit-packed draft masks (trees of up to 64 drafts) and the KV append
+# --------------------------------------------------------------------------
+def _numpy_reference(inp):
+    """The definition with numpy float64 dot products and this file's own visibility rule
+    (byte mask), exponentiating raw scores (small inputs): independent of the oracle."""
+    B, q, H = inp.B, inp.q_len, inp.H
+    out = np.zeros((B, q, H, 512))
+    lse = np.full((B, q, H), -math.inf)
+    for b in range(B):
+        for t in range(q):
+            vis = _visible(inp, b, t)
+            if not vis:
+                continue
+            K = np.stack([_f(inp.kv_bits[inp.slot_table[b, j]]) for j in vis])
+            for h in range(H):
+                e = np.exp(inp.scale * (K @ _f(inp.q_bits[b, t, h])))
+                lse[b, t, h] = math.log(e.sum())
+                out[b, t, h] = (e[:, None] * K[:, :512]).sum(0) / e.sum()
+    return out, lse
+
+
+def test_pack_mask_bits():
+    m = np.zeros((1, 64, 64), np.uint8)
+    m[0, 5, [0, 3, 63]] = 1
+    bits = w.pack_mask(m)
+    assert bits.dtype == np.uint64 and bits.shape == (1, 64)
+    assert int(bits[0, 5]) == (1 << 0) | (1 << 3) | (1 << 63) and int(bits[0, 4]) == 0
+
+
+@pytest.mark.parametrize("q_len,H", [(20, 2), (64, 1)])
+def test_packed_mask_equals_byte_mask_and_reference(q_len, H):
+    inp = w.make_verify("tree", 2, q_len, H, [3, 0], seed=40 + q_len, mask_kind="tree", draft_gain=50.0)
+    bits = w.pack_mask(inp.mask)
+    ob, lb = oracle.verify_inputs(inp, nthreads=2)
+    op, lp = oracle.verify(inp.q_bits, inp.kv_bits, inp.slot_table, inp.seq_lens, None, inp.scale,
+                           mask_bits=bits, nthreads=2)
+    assert np.array_equal(op, ob) and np.array_equal(lp, lb)
+    ro, rl = _numpy_reference(inp)
+    assert np.max(np.abs(op - ro)) < 1e-10 and np.max(np.abs(lp - rl)) < 1e-10
+
+
+def test_packed_null_mask_is_causal_chain():
+    inp = w.make_verify("chain", 1, 40, 1, [2], seed=44, mask_kind="none", draft_gain=50.0)
+    o0, l0 = oracle.verify_inputs(inp, nthreads=2)
+    o1, l1 = oracle.verify(inp.q_bits, inp.kv_bits, inp.slot_table, inp.seq_lens, None, inp.scale,
+                           mask_bits=None, nthreads=2)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    ro, rl = _numpy_reference(inp)
+    assert np.max(np.abs(o0 - ro)) < 1e-10
+
+
+def _draft_rows(inp):
+    rows = np.empty((inp.B, inp.q_len, 576), np.uint16)
+    for b in range(inp.B):
+        n = int(inp.seq_lens[b])
+        for i in range(inp.q_len):
+            rows[b, i] = inp.kv_bits[inp.slot_table[b, n - inp.q_len + i]]
+    return rows
+
+
+def test_kv_append_restores_generator_placement():
+    """Overwrite the drafts' pool rows with noise; appending the draft rows must give
+    back the generator's cache bit for bit, and touch no other row."""
+    inp = w.make_verify("app", 3, 9, 2, [30, 7, 0], seed=45, scattered=True, n_pool=400)
+    drafts = _draft_rows(inp)
+    noisy = inp.kv_bits.copy()
+    targets = sorted({int(inp.slot_table[b, int(inp.seq_lens[b]) - 9 + i]) for b in range(3) for i in range(9)})
+    noisy[targets] = np.random.default_rng(0).integers(0, 1 << 16, (len(targets), 576), dtype=np.uint16)
+    got = oracle.kv_append(noisy, inp.slot_table, inp.seq_lens, drafts)
+    assert np.array_equal(got, inp.kv_bits)
+    others = np.setdiff1d(np.arange(inp.n_pool), targets)
+    assert np.array_equal(got[others], noisy[others])
+
+
+def test_kv_append_rejects_bad_slot_or_length():
+    inp = w.make_verify("app", 1, 4, 1, [5], seed=46)
+    drafts = _draft_rows(inp)
+    st = inp.slot_table.copy()
+    st[0, int(inp.seq_lens[0]) - 1] = inp.n_pool
+    with pytest.raises(ValueError):
+        oracle.kv_append(inp.kv_bits, st, inp.seq_lens, drafts)
+    with pytest.raises(ValueError):
+        oracle.kv_append(inp.kv_bits, inp.slot_table, np.array([3], np.int32), drafts)

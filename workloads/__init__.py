@@ -162,6 +162,15 @@ def tree_mask_from_parents(par: np.ndarray) -> np.ndarray:
     return m
 
 
+def pack_mask(mask: np.ndarray) -> np.ndarray:
+    """uint8 [B, q, q] (mask[b, t, i] != 0: draft t sees draft i) -> uint64 [B, q] with
+    bit i of word (b, t) set for each seen draft (q <= 64).  A storage format only."""
+    B, q, q2 = mask.shape
+    assert q == q2 and q <= 64
+    bits = (np.asarray(mask) != 0).astype(np.uint64) << np.arange(q, dtype=np.uint64)
+    return np.bitwise_or.reduce(bits, axis=2).astype(np.uint64) if q else np.zeros((B, 0), np.uint64)
+
+
 # --------------------------------------------------------------------------
 # verify workloads
 # --------------------------------------------------------------------------

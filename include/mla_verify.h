@@ -72,7 +72,7 @@ typedef enum {
 /* Supported ranges. */
 #define MLA_D_QK 576           /* query / key width: 512 latent + 64 rope */
 #define MLA_D_V 512            /* value / output width */
-#define MLA_MAX_Q_LEN 16
+#define MLA_MAX_Q_LEN 64        /* drafts per stream: a draft tree of up to 64 nodes */
 #define MLA_MAX_HEADS 128
 #define MLA_MAX_NSPLIT 1024
 
@@ -110,7 +110,7 @@ int mla_verify_auto_nsplit(int B, int q_len, int H, int max_seq, int num_sms, si
  *   nsplit     0 = automatic (mla_verify_auto_nsplit), else 1..MLA_MAX_NSPLIT key splits
  *   workspace  device scratch of ws_bytes >= mla_verify_workspace_bytes(B,q_len,H,nsplit_used),
  *              256-byte aligned; may be NULL when the split count used is 1
- * Limits: 1 <= q_len <= 16, 1 <= H <= 128, 0 <= B <= 65535 (B == 0 is a no-op),
+ * Limits: 1 <= q_len <= 64, 1 <= H <= 128, 0 <= B <= 65535 (B == 0 is a no-op),
  *         1 <= n_pool <= 2^31 - 1, B * q_len * H <= 2^31 - 1.
  */
 int mla_verify_attn(const void* q, const void* kv_cache, int64_t n_pool,
@@ -118,6 +118,40 @@ int mla_verify_attn(const void* q, const void* kv_cache, int64_t n_pool,
                     const uint8_t* draft_mask, int B, int q_len, int H, float scale,
                     float* out, float* lse, int nsplit, void* workspace, size_t ws_bytes,
                     mla_stream_t stream);
+
+/*
+ * mla_verify_attn() with the draft mask bit-packed, for draft trees of up to 64
+ * nodes ("The Occupancy Epiphany: How One Environment Variable Unlocked 3x
+ * Throughput ...", sections "The Broader Context" and "Input Knowledge Required":
+ * DDTree draft trees verified in one pass).
+ *   draft_mask_bits uint64 [B, q_len], 8-byte aligned: bit i of word (b, t) set means
+ *                   draft t sees draft i (bits i >= q_len are ignored); NULL = causal chain
+ * Every other argument, limit and error is that of mla_verify_attn().
+ */
+int mla_verify_attn_packed(const void* q, const void* kv_cache, int64_t n_pool,
+                           const int32_t* slot_table, int slot_stride, const int32_t* seq_lens,
+                           const uint64_t* draft_mask_bits, int B, int q_len, int H, float scale,
+                           float* out, float* lse, int nsplit, void* workspace, size_t ws_bytes,
+                           mla_stream_t stream);
+
+/*
+ * KV append, the step before a verify call: the q_len new draft rows of every
+ * stream enter the paged latent cache.  Row i of stream b, new_kv[b, i, 0:576],
+ * is written to pool row slot_table[b, seq_lens[b] - q_len + i] (the drafts are
+ * the last q_len keys of the stream, as mla_verify_attn() reads them; the
+ * allocator's slots may be scattered: "The Occupancy Epiphany: How One
+ * Environment Variable ...", section "The Broader Context").
+ *   kv_cache   bf16 [n_pool, 576], 16-byte aligned, written in place
+ *   slot_table int32 [B, slot_stride]; seq_lens int32 [B] (as for mla_verify_attn)
+ *   new_kv     bf16 [B, q_len, 576], 16-byte aligned, read only
+ * The draft slots of one call must be distinct (otherwise which row lands in a
+ * shared slot is unspecified).  A stream whose seq_len is outside
+ * [q_len, slot_stride] is skipped and sets MLA_DEV_BAD_LEN; a slot outside
+ * [0, n_pool) skips that row and sets MLA_DEV_BAD_SLOT.
+ * Limits: 1 <= q_len <= 64, 0 <= B <= 65535, 1 <= n_pool <= 2^31 - 1.
+ */
+int mla_kv_append(void* kv_cache, int64_t n_pool, const int32_t* slot_table, int slot_stride,
+                  const int32_t* seq_lens, const void* new_kv, int B, int q_len, mla_stream_t stream);
 
 /*
  * The split stage of mla_verify_attn() alone: with nsplit >= 2 it writes the

@@ -20,7 +20,7 @@ from . import build as _build
 
 D_QK = 576
 D_V = 512
-MAX_Q_LEN = 16
+MAX_Q_LEN = 64
 MAX_HEADS = 128
 MAX_NSPLIT = 1024
 
@@ -33,7 +33,7 @@ DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
 EXPORTS = ("mla_verify_workspace_bytes", "mla_verify_auto_nsplit", "mla_verify_attn",
            "mla_verify_partials", "mla_verify_combine", "mla_verify_status",
            "mla_status_string", "mla_verify_version", "mla_verify_attn_static_scratch",
-           "mla_sparse_fp8_decode", "mla_sparse_fp8_partials")
+           "mla_sparse_fp8_decode", "mla_sparse_fp8_partials", "mla_verify_attn_packed", "mla_kv_append")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
@@ -65,7 +65,7 @@ def load():
     L.mla_verify_auto_nsplit.argtypes = [I, I, I, I, I, SZ]
     L.mla_verify_auto_nsplit.restype = I
     sig = [P, P, I64, P, I, P, P, I, I, I, F, P, P, I, P, SZ, P]
-    for fn in ("mla_verify_attn", "mla_verify_partials"):
+    for fn in ("mla_verify_attn", "mla_verify_partials", "mla_verify_attn_packed"):
         getattr(L, fn).argtypes = sig
         getattr(L, fn).restype = I
     fsig = [P, P, P, P, I64, P, I, I, I, F, P, P, I, P, SZ, P]
@@ -74,6 +74,8 @@ def load():
         getattr(L, fn).restype = I
     L.mla_verify_attn_static_scratch.argtypes = [P, P, I64, P, I, P, P, I, I, I, F, P, P, I, P]
     L.mla_verify_attn_static_scratch.restype = I
+    L.mla_kv_append.argtypes = [P, I64, P, I, P, P, I, I, P]
+    L.mla_kv_append.restype = I
     L.mla_verify_combine.argtypes = [P, P, I, I, I, I, P, P, P]
     L.mla_verify_combine.restype = I
     L.mla_verify_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I]
@@ -123,8 +125,13 @@ def _check_verify_tensors(q, kv_cache, slot_table, seq_lens, draft_mask):
     for t in (q, kv_cache, slot_table, seq_lens) + ((draft_mask,) if draft_mask is not None else ()):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("all tensors must be contiguous CUDA tensors")
+    if draft_mask is not None and draft_mask.dtype not in (torch.uint8, torch.int64):
+        raise TypeError("draft_mask must be uint8 [B, q_len, q_len] or bit-packed int64 [B, q_len]")
+
+
+def _byte_mask_only(draft_mask):
     if draft_mask is not None and draft_mask.dtype != torch.uint8:
-        raise TypeError("draft_mask must be uint8")
+        raise TypeError("this entry point takes the uint8 [B, q_len, q_len] mask (packed masks: verify_attn)")
 
 
 def verify_attn(q: torch.Tensor, kv_cache: torch.Tensor, slot_table: torch.Tensor, seq_lens: torch.Tensor,
@@ -133,8 +140,11 @@ def verify_attn(q: torch.Tensor, kv_cache: torch.Tensor, slot_table: torch.Tenso
                 stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """mla_verify_attn: out [B, q_len, H, 512] fp32 and lse [B, q_len, H] fp32.
 
-    ``workspace`` is a byte (uint8) CUDA tensor; when omitted, one sized for the
-    split count in use is allocated here (by torch, outside the library)."""
+    ``draft_mask`` is uint8 [B, q_len, q_len], or int64 [B, q_len] holding the
+    bit-packed mask (bit i of word (b, t): draft t sees draft i), which goes to
+    mla_verify_attn_packed; None means a causal chain.  ``workspace`` is a byte
+    (uint8) CUDA tensor; when omitted, one sized for the split count in use is
+    allocated here (by torch, outside the library)."""
     L = load()
     _check_verify_tensors(q, kv_cache, slot_table, seq_lens, draft_mask)
     B, q_len, H, _ = q.shape
@@ -145,11 +155,38 @@ def verify_attn(q: torch.Tensor, kv_cache: torch.Tensor, slot_table: torch.Tenso
     if workspace is None:
         ns = nsplit if nsplit > 0 else auto_nsplit(B, q_len, H, slot_table.shape[1], num_sms(q.device), 1 << 62)
         workspace = torch.empty(max(workspace_bytes(B, q_len, H, ns), 256), dtype=torch.uint8, device=q.device)
-    rc = L.mla_verify_attn(_ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(slot_table), slot_table.shape[1],
-                           _ptr(seq_lens), _ptr(draft_mask), B, q_len, H, float(scale), _ptr(out), _ptr(lse),
-                           nsplit, _ptr(workspace), workspace.numel(), _stream(stream))
-    _check("mla_verify_attn", rc)
+    packed = draft_mask is not None and draft_mask.dtype == torch.int64
+    if draft_mask is not None:
+        want = (B, q_len) if packed else (B, q_len, q_len)
+        if tuple(draft_mask.shape) != want:
+            raise ValueError(f"draft_mask must have shape {want}")
+    fn = "mla_verify_attn_packed" if packed else "mla_verify_attn"
+    rc = getattr(L, fn)(_ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(slot_table), slot_table.shape[1],
+                        _ptr(seq_lens), _ptr(draft_mask), B, q_len, H, float(scale), _ptr(out), _ptr(lse),
+                        nsplit, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(fn, rc)
     return out, lse
+
+
+def kv_append(kv_cache: torch.Tensor, slot_table: torch.Tensor, seq_lens: torch.Tensor, new_kv: torch.Tensor,
+              stream=None) -> torch.Tensor:
+    """mla_kv_append: writes new_kv [B, q_len, 576] (bf16) into kv_cache [n_pool, 576] at the
+    streams' draft slots (slot_table[b, seq_lens[b] - q_len + i]); returns kv_cache."""
+    L = load()
+    if kv_cache.dtype != torch.bfloat16 or new_kv.dtype != torch.bfloat16:
+        raise TypeError("kv_cache and new_kv must be bfloat16")
+    if kv_cache.dim() != 2 or kv_cache.shape[1] != D_QK or new_kv.dim() != 3 or new_kv.shape[2] != D_QK:
+        raise ValueError("kv_cache must be [n_pool, 576] and new_kv [B, q_len, 576]")
+    if slot_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("slot_table and seq_lens must be int32")
+    for t in (kv_cache, slot_table, seq_lens, new_kv):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    B, q_len, _ = new_kv.shape
+    rc = L.mla_kv_append(_ptr(kv_cache), kv_cache.shape[0], _ptr(slot_table), slot_table.shape[1], _ptr(seq_lens),
+                         _ptr(new_kv), B, q_len, _stream(stream))
+    _check("mla_kv_append", rc)
+    return kv_cache
 
 
 def verify_attn_static_scratch(q: torch.Tensor, kv_cache: torch.Tensor, slot_table: torch.Tensor,
@@ -162,6 +199,7 @@ def verify_attn_static_scratch(q: torch.Tensor, kv_cache: torch.Tensor, slot_tab
     overlaps share that array and race; the first call on a device sets it up."""
     L = load()
     _check_verify_tensors(q, kv_cache, slot_table, seq_lens, draft_mask)
+    _byte_mask_only(draft_mask)
     B, q_len, H, _ = q.shape
     if out is None:
         out = torch.empty((B, q_len, H, D_V), dtype=torch.float32, device=q.device)
@@ -223,6 +261,7 @@ def verify_partials(q, kv_cache, slot_table, seq_lens, draft_mask, scale, *, nsp
     workspace when nsplit > 1, else (out, lse)."""
     L = load()
     _check_verify_tensors(q, kv_cache, slot_table, seq_lens, draft_mask)
+    _byte_mask_only(draft_mask)
     B, q_len, H, _ = q.shape
     if out is None:
         out = torch.empty((B, q_len, H, D_V), dtype=torch.float32, device=q.device)

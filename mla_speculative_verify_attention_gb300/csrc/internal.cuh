@@ -25,6 +25,7 @@ struct VerifyArgs {
     int slot_stride;
     const int32_t* seq_lens;
     const uint8_t* mask;          // [B, q_len, q_len] or nullptr = causal chain
+    const uint64_t* mask_bits;    // [B, q_len] bit-packed mask (bit i: sees draft i); overrides mask
     int B, q_len, H;
     float scale;
     float* out;                   // [B, q_len, H, 512], used when nsplit == 1
@@ -61,6 +62,9 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
 // q_len * H rows, each padded to R (multiple of 16) MMA columns.
 void tc_tiling(int rows, int max_r, int* n_tiles, int* R_step, int* R);
 constexpr int TC_MAX_ROWS = 96;
+cudaError_t launch_kv_append(__nv_bfloat16* kv, const int32_t* slot, int slot_stride, const int32_t* seq_lens,
+                             const __nv_bfloat16* new_kv, int B, int q_len, int64_t n_pool, unsigned* status,
+                             cudaStream_t stream);
 cudaError_t launch_combine(const float* part_out, const float* part_lse, long long n_rows, int S,
                            float* out, float* lse, cudaStream_t stream);
 

@@ -167,8 +167,8 @@ int check_verify_args(const void* q, const void* kv, int64_t n_pool, const int32
 }
 
 int run_verify(bool combine, const void* q, const void* kv, int64_t n_pool, const int32_t* slot,
-               int slot_stride, const int32_t* seq_lens, const uint8_t* mask, int B, int q_len, int H,
-               float scale, float* out, float* lse, int nsplit, void* ws, size_t ws_bytes,
+               int slot_stride, const int32_t* seq_lens, const uint8_t* mask, const uint64_t* mask_bits, int B,
+               int q_len, int H, float scale, float* out, float* lse, int nsplit, void* ws, size_t ws_bytes,
                cudaStream_t stream) {
     int rc = check_verify_args(q, kv, n_pool, slot, slot_stride, seq_lens, B, q_len, H, scale, out, lse, nsplit);
     if (rc != MLA_OK) return rc;
@@ -189,6 +189,7 @@ int run_verify(bool combine, const void* q, const void* kv, int64_t n_pool, cons
     a.slot_stride = slot_stride;
     a.seq_lens = seq_lens;
     a.mask = mask;
+    a.mask_bits = mask_bits;
     a.B = B; a.q_len = q_len; a.H = H;
     a.scale = scale;
     a.out = out; a.lse = lse;
@@ -301,16 +302,43 @@ int mla_verify_attn(const void* q, const void* kv_cache, int64_t n_pool, const i
                     int slot_stride, const int32_t* seq_lens, const uint8_t* draft_mask, int B, int q_len,
                     int H, float scale, float* out, float* lse, int nsplit, void* workspace, size_t ws_bytes,
                     mla_stream_t stream) {
-    return run_verify(true, q, kv_cache, n_pool, slot_table, slot_stride, seq_lens, draft_mask, B, q_len, H,
-                      scale, out, lse, nsplit, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+    return run_verify(true, q, kv_cache, n_pool, slot_table, slot_stride, seq_lens, draft_mask, nullptr, B, q_len,
+                      H, scale, out, lse, nsplit, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_verify_attn_packed(const void* q, const void* kv_cache, int64_t n_pool, const int32_t* slot_table,
+                           int slot_stride, const int32_t* seq_lens, const uint64_t* draft_mask_bits, int B,
+                           int q_len, int H, float scale, float* out, float* lse, int nsplit, void* workspace,
+                           size_t ws_bytes, mla_stream_t stream) {
+    if (draft_mask_bits && (reinterpret_cast<uintptr_t>(draft_mask_bits) % 8) != 0) return MLA_ERR_ALIGN;
+    return run_verify(true, q, kv_cache, n_pool, slot_table, slot_stride, seq_lens, nullptr, draft_mask_bits, B,
+                      q_len, H, scale, out, lse, nsplit, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_kv_append(void* kv_cache, int64_t n_pool, const int32_t* slot_table, int slot_stride,
+                  const int32_t* seq_lens, const void* new_kv, int B, int q_len, mla_stream_t stream) {
+    if (B < 0 || B > 65535 || q_len < 1 || q_len > MLA_MAX_Q_LEN) return MLA_ERR_SHAPE;
+    if (B == 0) return MLA_OK;
+    if (!kv_cache || !slot_table || !seq_lens || !new_kv) return MLA_ERR_NULL;
+    if (n_pool < 1 || n_pool > 0x7fffffffLL || slot_stride < q_len) return MLA_ERR_SHAPE;
+    if (!aligned(kv_cache, 16) || !aligned(new_kv, 16) || !aligned(slot_table, 4) || !aligned(seq_lens, 4))
+        return MLA_ERR_ALIGN;
+    unsigned* status = nullptr;
+    int rc = device_state(nullptr, &status, nullptr);
+    if (rc != MLA_OK) return rc;
+    if (launch_kv_append(static_cast<__nv_bfloat16*>(kv_cache), slot_table, slot_stride, seq_lens,
+                         static_cast<const __nv_bfloat16*>(new_kv), B, q_len, n_pool, status,
+                         reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MLA_ERR_LAUNCH;
+    return MLA_OK;
 }
 
 int mla_verify_partials(const void* q, const void* kv_cache, int64_t n_pool, const int32_t* slot_table,
                         int slot_stride, const int32_t* seq_lens, const uint8_t* draft_mask, int B, int q_len,
                         int H, float scale, float* out, float* lse, int nsplit, void* workspace,
                         size_t ws_bytes, mla_stream_t stream) {
-    return run_verify(false, q, kv_cache, n_pool, slot_table, slot_stride, seq_lens, draft_mask, B, q_len, H,
-                      scale, out, lse, nsplit, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+    return run_verify(false, q, kv_cache, n_pool, slot_table, slot_stride, seq_lens, draft_mask, nullptr, B, q_len,
+                      H, scale, out, lse, nsplit, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mla_verify_combine(const float* part_out, const float* part_lse, int B, int q_len, int H, int S, float* out,

@@ -377,12 +377,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const bool row_ok = r < nrows;
         const int t = row_ok ? (row0 + r) / a.H : 0;
-        unsigned vis = 0;
-        if (row_ok)
-            for (int d = 0; d < a.q_len; ++d) {
-                const bool seen = a.mask ? a.mask[((int64_t)b * a.q_len + t) * a.q_len + d] != 0 : d <= t;
-                vis |= (seen ? 1u : 0u) << d;
+        // drafts this row sees, bit i = draft i (q_len <= 64)
+        uint64_t vis = 0;
+        if (row_ok) {
+            if (a.mask_bits) {
+                vis = a.mask_bits[(int64_t)b * a.q_len + t];
+            } else {
+                for (int d = 0; d < a.q_len; ++d) {
+                    const bool seen = a.mask ? a.mask[((int64_t)b * a.q_len + t) * a.q_len + d] != 0 : d <= t;
+                    vis |= (uint64_t)(seen ? 1u : 0u) << d;
+                }
             }
+        }
         if (T > 0) {
             // Q chunks 0 .. nq_t-1 of row r into TMEM lane r (rows past the tile: zeros),
             // two chunks (sixteen 16-byte loads) in flight at a time
@@ -453,7 +459,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int k = 0; k < NK; ++k) {
                     const int j = k0 + k;
-                    const bool vk = row_ok && j < k_end && (j < p || ((vis >> (j - p)) & 1u));
+                    const bool vk = row_ok && j < k_end && (j < p || ((vis >> (j - p)) & 1ull));
                     x[k] = vk ? __uint_as_float(sv[k]) * c2 : -INFINITY;
                     mt = fmaxf(mt, x[k]);
                 }

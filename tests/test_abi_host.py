@@ -78,7 +78,7 @@ def _call_attn(lib, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), -1), (dict(kv=None), -1), (dict(slot=None), -1), (dict(out=None), -1),
-    (dict(q_len=0), -2), (dict(q_len=17), -2), (dict(H=0), -2), (dict(H=129), -2),
+    (dict(q_len=0), -2), (dict(q_len=65), -2), (dict(H=0), -2), (dict(H=129), -2),
     (dict(stride=8), -2), (dict(n_pool=0), -2),
     (dict(q=24), -3), (dict(out=20), -3), (dict(slot=18), -3),
     (dict(nsplit=-1), -5), (dict(nsplit=1025), -5),
@@ -122,3 +122,19 @@ def test_combine_argument_errors(lib):
     assert lib.mla_verify_combine(P(16), P(16), 1, 9, 8, 0, P(16), P(16), None) == -5
     assert lib.mla_verify_combine(P(16), P(16), 1, 0, 8, 4, P(16), P(16), None) == -2
     assert lib.mla_verify_combine(P(8), P(16), 1, 9, 8, 4, P(16), P(16), None) == -3
+
+
+def test_packed_and_append_argument_errors(lib):
+    P = ctypes.c_void_p
+    f = lib.mla_verify_attn_packed
+    def call(mask=16, q_len=9, q=16):
+        return f(P(q), P(16), 10, P(16), 64, P(16), P(mask), 1, q_len, 8, 0.1, P(16), P(16), 1, None, 0, None)
+    assert call(mask=12) == -3                             # mask words must be 8-byte aligned
+    assert call(q_len=65) == -2 and call(q=None) == -1
+    g = lib.mla_kv_append
+    def app(kv=16, new=16, B=2, q_len=9, stride=16, n_pool=10):
+        return g(P(kv), n_pool, P(16), stride, P(16), P(new), B, q_len, None)
+    assert app(kv=None) == -1 and app(new=None) == -1
+    assert app(q_len=0) == -2 and app(q_len=65) == -2 and app(stride=8) == -2 and app(n_pool=0) == -2
+    assert app(kv=8) == -3 and app(new=24) == -3
+    assert app(B=0, kv=None) == 0

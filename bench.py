@@ -3,15 +3,19 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl reference]
 
-Prints ONE JSON line.  A step is one verify call (split kernel + combine) over
-one synthetic batch of the named workload (default c2: 1 stream, q_len 9, H 64,
-prefix 4096, contiguous slots, causal chain -- the pages' microbenchmark shape).
-`value` is effective KV bandwidth (KV-row bytes / time) with inputs resident in
-HBM, timed with CUDA events per step on the launching stream; L2 is flushed
-(256 MiB written) before every step, outside the events.  `e2e` is the same
-metric with the step's inputs copied from pinned host memory and the outputs
-copied back inside the timed region.  `--impl reference` times the fp64 CPU
-oracle on this host's cores instead (the reference arm).
+Prints ONE JSON line.  A step is one verify call through the C ABI
+(mla_verify_attn: split kernel + combine) over one synthetic batch of the named
+workload (default c2: 1 stream, q_len 9, H 64, prefix 4096, contiguous slots,
+causal chain -- the pages' microbenchmark shape).  `value` is effective KV
+bandwidth (KV-row bytes / time) with inputs resident in HBM, timed with CUDA
+events per step on the launching stream; L2 is flushed (256 MiB written) before
+every step, outside the events.  The split kernel alone is timed the same way in
+a second loop (its duration is the roofline's denominator), and a warm-L2 loop
+(no flush) is reported beside it.  `e2e` is the same metric end to end: the
+step's inputs (queries, slot table, lengths, mask and the new draft KV rows)
+copied from pinned host memory, the KV append kernel, the verify call and the
+outputs copied back, all inside the timed region.  `--impl reference` times the
+fp64 CPU oracle on this host's cores instead (the reference arm).
 """
 from __future__ import annotations
 
@@ -284,8 +288,9 @@ class VerifyWorkload:
                             nsplit=ns, workspace=ws, stream=stream)
 
     def host_inputs(self):
-        """(pinned host tensor, device view to fill) pairs: queries, slot table, lengths, mask
-        and the q_len new draft KV rows of every stream (written into their pool slots)."""
+        """(pinned host tensor, device tensor to fill) pairs: queries, slot table, lengths,
+        mask and the q_len new draft KV rows of every stream ([B, q_len, 576], staged for
+        the KV append kernel, which writes them into their pool slots)."""
         import torch
         inp = self.inp
         pairs = [(torch.from_numpy(inp.q_bits.view(np.int16)).pin_memory(), self.q.view(torch.int16)),
@@ -293,17 +298,18 @@ class VerifyWorkload:
                  (torch.from_numpy(np.ascontiguousarray(inp.seq_lens)).pin_memory(), self.sl)]
         if self.mk is not None:
             pairs.append((torch.from_numpy(np.ascontiguousarray(inp.mask)).pin_memory(), self.mk))
-        kv16 = self.kv.view(torch.int16)
+        rows = np.empty((inp.B, inp.q_len, 576), np.uint16)
         for b in range(inp.B):
-            s = inp.slot_table[b, inp.seq_lens[b] - inp.q_len:inp.seq_lens[b]]
-            start = 0
-            for k in range(1, len(s) + 1):          # contiguous runs of draft slots: one copy each
-                if k == len(s) or s[k] != s[k - 1] + 1:
-                    rows = np.arange(s[start], s[start] + (k - start))
-                    pairs.append((torch.from_numpy(inp.kv_bits[rows].view(np.int16)).pin_memory(),
-                                  kv16[int(s[start]):int(s[start]) + (k - start)]))
-                    start = k
+            n = int(inp.seq_lens[b])
+            rows[b] = inp.kv_bits[inp.slot_table[b, n - inp.q_len:n]]
+        self.new_rows = torch.empty(rows.shape, dtype=torch.bfloat16, device=self.dev)
+        pairs.append((torch.from_numpy(rows.view(np.int16)).pin_memory(), self.new_rows.view(torch.int16)))
         return pairs
+
+    def before_call(self, stream):
+        """KV append of the staged draft rows (end-to-end step only); returns launches."""
+        self.mv.kv_append(self.kv, self.st, self.sl, self.new_rows, stream=stream)
+        return 1
 
     def oracle_call(self, threads):
         import oracle
@@ -345,6 +351,9 @@ class Fp8Workload:
             pairs.append((torch.from_numpy(f.kv_rope[r:r + 1].view(np.int16).copy()).pin_memory(),
                           self.rope.view(torch.int16)[r:r + 1]))
         return pairs
+
+    def before_call(self, stream):
+        return 0
 
     def oracle_call(self, threads):
         import oracle
@@ -393,44 +402,49 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     launches_per_step = 1 + (1 if ns > 1 else 0)
 
-    def step(e0=None, e1=None, e2=None):
-        if e0 is not None:
-            e0.record(stream)
-        res = wl.partials(ns, ws, out, lse, stream)
-        if e1 is not None:
-            e1.record(stream)
-        if ns > 1:
-            po, pl = res
-            mv.verify_combine(po, pl, B, q_len, H, out=out, lse=lse, stream=stream)
-        if e2 is not None:
-            e2.record(stream)
+    def timed_loop(n, fn, flush_l2=True):
+        """n calls of fn(), each bracketed by CUDA events on the launching stream; L2 flushed
+        before each call (outside the events) unless flush_l2 is False.  Returns ms per call."""
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        torch.cuda.synchronize(dev)
+        for i in range(n):
+            if flush_l2:
+                flush.fill_(float(i))
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def full_call():
+        wl.full(ns, ws, out, lse, stream)
+
+    def split_kernel():
+        wl.partials(ns, ws, out, lse, stream)
 
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1.0)
-        step()
+        full_call()
+        split_kernel()
     torch.cuda.synchronize(dev)
 
     clocks = Clocks(local)
     clocks.start()
     time.sleep(0.25)
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    for i in range(K):
-        flush.fill_(float(i))
-        step(*ev[i])
-    torch.cuda.synchronize(dev)
+    step_ms = timed_loop(K, full_call)                     # the timed region: K whole verify calls
     wall_dev = time.perf_counter() - wall0
-    step_ms = [a.elapsed_time(c) for a, b, c in ev]
-    kern_ms = [a.elapsed_time(b) for a, b, c in ev]
+    kern_ms = timed_loop(min(K, 500), split_kernel)        # the split (attention) kernel alone
+    warm_ms = timed_loop(min(K, 200), full_call, flush_l2=False)
     status = mv.device_status(stream)
 
     # end to end through the C ABI with host buffers: this step's inputs copied from
-    # pinned memory, the call (mla_verify_attn / mla_sparse_fp8_decode), and D2H of out
-    # and lse, all inside the events
+    # pinned memory, the KV append (verify path), the call (mla_verify_attn /
+    # mla_sparse_fp8_decode), and D2H of out and lse, all inside the events
     pairs = wl.host_inputs()
     h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
@@ -440,29 +454,23 @@ def run_gpu(args):
     def e2e_step():
         for h, d in pairs:
             d.copy_(h, non_blocking=True)
+        wl.before_call(stream)
         wl.full(ns, ws, out, lse, stream)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
-    Ke = max(1, min(K, 200))
-    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
-    torch.cuda.synchronize(dev)
-    for i in range(Ke):
-        flush.fill_(float(i))
-        ee[i][0].record(stream)
-        e2e_step()
-        ee[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = [a.elapsed_time(b) for a, b in ee]
+    e2e_ms = timed_loop(max(1, min(K, 200)), e2e_step)
     clk = clocks.stop()
 
     # aggregate over ranks: max time, summed work
     mean_step = statistics.mean(step_ms)
     mean_kern = statistics.mean(kern_ms)
     mean_e2e = statistics.mean(e2e_ms)
-    mean_step, mean_kern, mean_e2e = max_over_ranks([mean_step, mean_kern, mean_e2e], device=dev)
+    mean_warm = statistics.mean(warm_ms)
+    mean_step, mean_kern, mean_e2e, mean_warm = max_over_ranks([mean_step, mean_kern, mean_e2e, mean_warm],
+                                                               device=dev)
     value = aggregate_throughput(work["kv_bytes"], mean_step, world)
     e2e_value = aggregate_throughput(work["kv_bytes"], mean_e2e, world)
 
@@ -493,6 +501,7 @@ def run_gpu(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "us_per_call": mean_step * 1e3,
         "us_per_call_p10_p50_p90": [srt[int(0.1 * (K - 1))] * 1e3, srt[(K - 1) // 2] * 1e3, srt[int(0.9 * (K - 1))] * 1e3],
+        "us_per_call_warm_l2": mean_warm * 1e3,
         "roofline_us": rl_us, "roofline_pct": 100.0 * rl_us / (mean_step * 1e3),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": traffic_from_profiles(args.config), "kernel": "split (attention) kernel",

@@ -394,8 +394,19 @@ def run_gpu(args):
     peaks = load_peaks()
     rl_us, bound, t_mem, t_mma = roofline_us(work, peaks["hbm_gbs"], peaks["bf16_tflops"])
     B, q_len, H = wl.B, wl.q_len, wl.H
+    # workspace for the automatic split count; the calls pass --nsplit (0 = automatic, which
+    # for 2..64 streams is the balanced split over one wave of CTAs when it fits)
     ns = args.nsplit or mv.auto_nsplit(B, q_len, H, wl.max_seq, mv.num_sms(dev), 1 << 62)
     ws = torch.empty(max(mv.workspace_bytes(B, q_len, H, ns), 256), dtype=torch.uint8, device=dev)
+    call_ns = args.nsplit
+    split_desc = f"uniform, {ns} per stream"
+    if call_ns == 0 and not isinstance(wl, Fp8Workload) and 2 <= B <= 64:
+        tiles = -(-(q_len * H) // 96)
+        slots = mv.num_sms(dev) // tiles
+        need = -(-(slots * q_len * H * 512 * 4) // 256) * 256 + -(-(slots * q_len * H * 4) // 256) * 256
+        if slots - B >= B and need <= ws.numel():
+            split_desc = f"balanced, {slots} slots over all streams (one wave)"
+            ns = slots
     out = torch.empty((B, q_len, H, 512), dtype=torch.float32, device=dev)
     lse = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -417,10 +428,10 @@ def run_gpu(args):
         return [a.elapsed_time(b) for a, b in ev]
 
     def full_call():
-        wl.full(ns, ws, out, lse, stream)
+        wl.full(call_ns, ws, out, lse, stream)
 
     def split_kernel():
-        wl.partials(ns, ws, out, lse, stream)
+        wl.partials(call_ns, ws, out, lse, stream)
 
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1.0)
@@ -455,7 +466,7 @@ def run_gpu(args):
         for h, d in pairs:
             d.copy_(h, non_blocking=True)
         wl.before_call(stream)
-        wl.full(ns, ws, out, lse, stream)
+        wl.full(call_ns, ws, out, lse, stream)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
@@ -496,7 +507,7 @@ def run_gpu(args):
         "vs_baseline": (PAGES_C2_US / (mean_step * 1e3)) if args.config == "c2" and world == 1 else None,
         "dtype": "bf16", "data": "synthetic (seeded SplitMix64 / Box-Muller inputs, shapes of the pages' workloads)",
         "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "B": B, "q_len": q_len,
-                   "H": H, "keys": work["keys"], "nsplit": ns,
+                   "H": H, "keys": work["keys"], "nsplit": ns, "split": split_desc,
                    "l2": "flushed before every step (256 MiB write, outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "us_per_call": mean_step * 1e3,

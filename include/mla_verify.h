@@ -162,7 +162,12 @@ int mla_kv_append(void* kv_cache, int64_t n_pool, const int32_t* slot_table, int
  * [s*c, (s+1)*c) intersected with [0, n), where c = ceil(n / nsplit) rounded up
  * to a multiple of 32; trailing splits may be empty (lse = -inf, out = 0).
  * mla_verify_partials() followed by mla_verify_combine() on the workspace
- * sections is exactly mla_verify_attn().
+ * sections is exactly mla_verify_attn() with the same nsplit.
+ * nsplit == 0 runs the split stage exactly as mla_verify_attn() with nsplit = 0
+ * would, including the balanced split it picks for 2..64 streams (all streams'
+ * keys cut into equal chunks over one wave of CTAs, chosen on the device from
+ * seq_lens); the partials' layout is then internal: use it to time the split stage
+ * of an automatic call, not as input to mla_verify_combine().
  */
 int mla_verify_partials(const void* q, const void* kv_cache, int64_t n_pool,
                         const int32_t* slot_table, int slot_stride, const int32_t* seq_lens,

@@ -256,9 +256,10 @@ def sparse_fp8_decode(q, kv_lat, kv_scale, kv_rope, topk_slots, scale, *, out=No
 def verify_partials(q, kv_cache, slot_table, seq_lens, draft_mask, scale, *, nsplit: int,
                     workspace: torch.Tensor, out: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None, stream=None):
-    """mla_verify_partials: the split stage alone (nsplit >= 1 explicit).  Returns
-    (part_out [B*q_len*H, nsplit, 512], part_lse [B*q_len*H, nsplit]) views of the
-    workspace when nsplit > 1, else (out, lse)."""
+    """mla_verify_partials: the split stage alone.  Returns (part_out [B*q_len*H, nsplit,
+    512], part_lse [B*q_len*H, nsplit]) views of the workspace when nsplit > 1, (out, lse)
+    when nsplit == 1, and None when nsplit == 0 (the automatic call's split stage, whose
+    partial layout is internal: for timing)."""
     L = load()
     _check_verify_tensors(q, kv_cache, slot_table, seq_lens, draft_mask)
     _byte_mask_only(draft_mask)
@@ -271,6 +272,8 @@ def verify_partials(q, kv_cache, slot_table, seq_lens, draft_mask, scale, *, nsp
                                _ptr(seq_lens), _ptr(draft_mask), B, q_len, H, float(scale), _ptr(out), _ptr(lse),
                                nsplit, _ptr(workspace), workspace.numel(), _stream(stream))
     _check("mla_verify_partials", rc)
+    if nsplit == 0:
+        return None
     if nsplit == 1:
         return out, lse
     return workspace_views(workspace, B, q_len, H, nsplit)

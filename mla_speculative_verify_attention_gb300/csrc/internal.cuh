@@ -32,8 +32,13 @@ struct VerifyArgs {
     float* lse;                   // [B, q_len, H]
     float* part_out;              // [B, q_len, H, nsplit, 512], used when nsplit > 1
     float* part_lse;              // [B, q_len, H, nsplit]
-    int nsplit;
+    int nsplit;                   // uniform splits per stream, or (balanced) split slots
     unsigned* status;             // device status word
+    // balanced split (several streams of unequal length, see balanced_plan): grid.x =
+    // nsplit slots shared by all streams; partials are slot-major,
+    // part_out [nsplit][q_len * H][512], part_lse [nsplit][q_len * H]
+    int balanced;
+    int bal_G;
     // fp8 sparse decode (kv_fp8 != 0): keys come from per-stream index lists
     // (slot = topk_slots [B, slot_stride = topk], seq_lens unused, q_len = 1) and
     // each key row is an e4m3 latent [512] with a per-token fp32 scale plus a bf16
@@ -56,6 +61,85 @@ __host__ __device__ inline void split_range(int n, int S, int s, int tile, int* 
     *end = (int)(e < n ? e : n);
 }
 
+// Balanced key split of one launch over B <= 64 streams of unequal length, decided on
+// the device (the host does not know the lengths): with T the sum of the valid lengths,
+// the keys are cut into chunks of chunk = max(128, ceil(T / G) rounded up to 32) keys;
+// stream b gets ns_b = ceil(n_b / chunk) consecutive split slots (one for a stream whose
+// length is invalid, which then writes NaN), slots numbered stream after stream, at
+// most G + B of them.  Every warp evaluates it alike (lane i holds streams i and
+// i + 32), so no barrier or shared memory is needed.
+struct BalancedPlan {
+    int chunk;
+    int ns[2];      // split slots of streams lane and lane + 32
+    int incl[2];    // inclusive prefix sums of the slot counts at those streams
+};
+
+__device__ inline BalancedPlan balanced_plan(const int32_t* seq_lens, int B, int q_len, int slot_stride, int G) {
+    const int lane = threadIdx.x & 31;
+    BalancedPlan P;
+    int n[2];
+    bool ok[2];
+    long long t = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        n[h] = i < B ? seq_lens[i] : 0;
+        ok[h] = i < B && n[h] >= q_len && n[h] <= slot_stride;
+        if (ok[h]) t += n[h];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    long long c = (t + G - 1) / G;
+    c = (c + 31) / 32 * 32;
+    if (c < 128) c = 128;
+    if (c > (1 << 30)) c = 1 << 30;
+    P.chunk = (int)c;
+    int run = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        P.ns[h] = i < B ? (ok[h] ? (int)(((long long)n[h] + c - 1) / c) : 1) : 0;
+        int v = P.ns[h];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+        }
+        P.incl[h] = v + run;
+        run += __shfl_sync(0xffffffffu, v, 31);
+    }
+    return P;
+}
+
+// Stream and split of slot x (b = -1: slot unused).  Whole warp.
+__device__ inline void balanced_slot(const BalancedPlan& P, int x, int* b, int* s) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const unsigned m = __ballot_sync(0xffffffffu, x < P.incl[h]);
+        if (m) {
+            const int L = __ffs(m) - 1;
+            const int incl = __shfl_sync(0xffffffffu, P.incl[h], L);
+            const int ns = __shfl_sync(0xffffffffu, P.ns[h], L);
+            *b = L + 32 * h;
+            *s = x - (incl - ns);
+            return;
+        }
+    }
+    *b = -1;
+    *s = 0;
+}
+
+// First slot and slot count of stream b (0 <= b < B <= 64).  Whole warp.
+__device__ inline void balanced_stream(const BalancedPlan& P, int b, int* first, int* count) {
+    const int h = b >> 5, L = b & 31;
+    const int incl = __shfl_sync(0xffffffffu, h ? P.incl[1] : P.incl[0], L);
+    const int ns = __shfl_sync(0xffffffffu, h ? P.ns[1] : P.ns[0], L);
+    *first = incl - ns;
+    *count = ns;
+}
+
+constexpr int BALANCED_MAX_STREAMS = 64;
+
 // Launchers (each returns the cudaError_t of the launch).
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
 // Row tiling of the tensor-core split kernel: n_tiles CTAs of R_step rows over
@@ -67,5 +151,7 @@ cudaError_t launch_kv_append(__nv_bfloat16* kv, const int32_t* slot, int slot_st
                              cudaStream_t stream);
 cudaError_t launch_combine(const float* part_out, const float* part_lse, long long n_rows, int S,
                            float* out, float* lse, cudaStream_t stream);
+// Combine of a balanced split (slot-major partials of VerifyArgs::balanced).
+cudaError_t launch_combine_balanced(const VerifyArgs& a, cudaStream_t stream);
 
 }  // namespace mla

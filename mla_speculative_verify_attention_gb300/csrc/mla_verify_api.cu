@@ -60,9 +60,18 @@ constexpr int CB_THREADS = 256;
 constexpr int CB_DIMS = 128;
 constexpr int CB_GROUPS = CB_THREADS / 32;
 
+// Balanced partials (slot-major): the row's splits are slots first .. first + count - 1
+// of its stream, recomputed from the lengths exactly as the split kernel chose them.
+struct CombineBalanced {
+    int on;
+    const int32_t* seq_lens;
+    int B, q_len, slot_stride, G, rows;
+};
+
 __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __restrict__ part_out,
                                                              const float* __restrict__ part_lse, int S,
-                                                             float* __restrict__ out, float* __restrict__ lse) {
+                                                             float* __restrict__ out, float* __restrict__ lse,
+                                                             const CombineBalanced bal) {
     extern __shared__ float wsm[];                  // [S] split weights
     __shared__ float4 acc_s[CB_GROUPS][32];
     __shared__ float row_stat[2];                   // lse, state (0 ok, 1 empty, 2 malformed)
@@ -70,13 +79,27 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __rest
     const int tid = threadIdx.x, lane = tid & 31, g = tid >> 5;
     const long long row = blockIdx.x;
     const int quarter = blockIdx.y;
+    // split s of this row: lse at pl[s * lse_step], output at po_row + s * out_step
+    long long lse_step = 1, out_step = D_V;
     const float* pl = part_lse + row * S;
+    const float* po_row = part_out + row * (long long)S * D_V;
+    if (bal.on) {
+        const BalancedPlan P = balanced_plan(bal.seq_lens, bal.B, bal.q_len, bal.slot_stride, bal.G);
+        const int b = (int)(row / bal.rows), r = (int)(row % bal.rows);
+        int first, count;
+        balanced_stream(P, b, &first, &count);
+        S = count;
+        lse_step = bal.rows;
+        out_step = (long long)bal.rows * D_V;
+        pl = part_lse + (long long)first * bal.rows + r;
+        po_row = part_out + ((long long)first * bal.rows + r) * D_V;
+    }
 
     if (g == 0) {
         float mx = -INFINITY;
         bool bad = false;
         for (int s = lane; s < S; s += 32) {
-            const float v = pl[s];
+            const float v = pl[s * lse_step];
             bad |= v != v;
             mx = fmaxf(mx, v);
         }
@@ -85,11 +108,11 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __rest
         bad = __any_sync(0xffffffffu, bad);
         float z = 0.f;
         if (!bad && mx != -INFINITY)
-            for (int s = lane; s < S; s += 32) z += expf(pl[s] - mx);
+            for (int s = lane; s < S; s += 32) z += expf(pl[s * lse_step] - mx);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         const float L = mx + logf(z);
-        for (int s = lane; s < S; s += 32) wsm[s] = (bad || mx == -INFINITY) ? 0.f : expf(pl[s] - L);
+        for (int s = lane; s < S; s += 32) wsm[s] = (bad || mx == -INFINITY) ? 0.f : expf(pl[s * lse_step] - L);
         if (lane == 0) {
             row_stat[0] = bad ? __int_as_float(0x7fc00000) : (mx == -INFINITY ? -INFINITY : L);
             row_stat[1] = bad ? 2.f : (mx == -INFINITY ? 1.f : 0.f);
@@ -98,12 +121,12 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __rest
     __syncthreads();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (row_stat[1] == 0.f) {
-        const float* base = part_out + row * (long long)S * D_V + quarter * CB_DIMS + lane * 4;
+        const float* base = po_row + quarter * CB_DIMS + lane * 4;
 #pragma unroll 4
         for (int s = g; s < S; s += CB_GROUPS) {
             const float w = wsm[s];
             if (w == 0.f) continue;
-            const float4 v = *reinterpret_cast<const float4*>(base + (long long)s * D_V);
+            const float4 v = *reinterpret_cast<const float4*>(base + (long long)s * out_step);
             acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
         }
     }
@@ -123,8 +146,8 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __rest
 
 }  // namespace
 
-cudaError_t launch_combine(const float* part_out, const float* part_lse, long long n_rows, int S,
-                           float* out, float* lse, cudaStream_t stream) {
+static cudaError_t launch_combine_any(const float* part_out, const float* part_lse, long long n_rows, int S,
+                                      float* out, float* lse, const CombineBalanced& bal, cudaStream_t stream) {
     if (n_rows <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)n_rows, D_V / CB_DIMS);
@@ -136,7 +159,25 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, long lo
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, part_out, part_lse, S, out, lse);
+    return cudaLaunchKernelEx(&cfg, combine_kernel, part_out, part_lse, S, out, lse, bal);
+}
+
+cudaError_t launch_combine(const float* part_out, const float* part_lse, long long n_rows, int S,
+                           float* out, float* lse, cudaStream_t stream) {
+    CombineBalanced off;
+    memset(&off, 0, sizeof off);
+    return launch_combine_any(part_out, part_lse, n_rows, S, out, lse, off, stream);
+}
+
+// S here bounds the slots of one stream (nsplit slots in all): the weights' shared memory.
+cudaError_t launch_combine_balanced(const VerifyArgs& a, cudaStream_t stream) {
+    CombineBalanced bal;
+    bal.on = 1;
+    bal.seq_lens = a.seq_lens;
+    bal.B = a.B; bal.q_len = a.q_len; bal.slot_stride = a.slot_stride; bal.G = a.bal_G;
+    bal.rows = a.q_len * a.H;
+    return launch_combine_any(a.part_out, a.part_lse, (long long)a.B * bal.rows, a.nsplit, a.out, a.lse, bal,
+                              stream);
 }
 
 }  // namespace mla
@@ -172,7 +213,6 @@ int run_verify(bool combine, const void* q, const void* kv, int64_t n_pool, cons
                cudaStream_t stream) {
     int rc = check_verify_args(q, kv, n_pool, slot, slot_stride, seq_lens, B, q_len, H, scale, out, lse, nsplit);
     if (rc != MLA_OK) return rc;
-    if (!combine && nsplit == 0) return MLA_ERR_NSPLIT;
     if (B == 0) return MLA_OK;
     unsigned* status = nullptr;
     int num_sms = 0;
@@ -195,6 +235,26 @@ int run_verify(bool combine, const void* q, const void* kv, int64_t n_pool, cons
     a.out = out; a.lse = lse;
     a.nsplit = ns;
     a.status = status;
+    // Several streams of unequal length with the automatic split count: cut all their
+    // keys into equal chunks over one wave of CTAs (balanced split) when the workspace
+    // holds its slot-major partials; the uniform per-stream split otherwise.
+    if (nsplit == 0 && B >= 2 && B <= BALANCED_MAX_STREAMS && ws && aligned(ws, 256)) {
+        int n_tiles, R_step, R;
+        tc_tiling(q_len * H, TC_MAX_ROWS, &n_tiles, &R_step, &R);
+        const long long slots = num_sms / n_tiles;
+        const long long per_stream = (long long)q_len * H;
+        const size_t need = align256((size_t)slots * per_stream * D_V * 4) + align256((size_t)slots * per_stream * 4);
+        if (slots - B >= B && need <= ws_bytes) {
+            a.balanced = 1;
+            a.bal_G = (int)(slots - B);
+            a.nsplit = (int)slots;
+            a.part_out = static_cast<float*>(ws);
+            a.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)slots * per_stream * D_V * 4));
+            if (launch_verify_tc(a, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+            if (combine && launch_combine_balanced(a, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+            return MLA_OK;
+        }
+    }
     if (ns > 1) {
         size_t need = mla_verify_workspace_bytes(B, q_len, H, ns);
         if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
@@ -213,7 +273,6 @@ int run_sparse_fp8(bool combine, const void* q, const uint8_t* kv_lat, const flo
                    float* lse, int nsplit, void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (B < 0 || B > 65535 || H < 1 || H > MLA_MAX_HEADS) return MLA_ERR_SHAPE;
     if (nsplit < 0 || nsplit > MLA_MAX_NSPLIT) return MLA_ERR_NSPLIT;
-    if (!combine && nsplit == 0) return MLA_ERR_NSPLIT;
     if (B == 0) return MLA_OK;
     if (!q || !kv_lat || !kv_scale || !kv_rope || !topk_slots || !out || !lse) return MLA_ERR_NULL;
     if (topk < 1 || n_pool < 1 || n_pool > 0x7fffffffLL || (long long)B * H > 0x7fffffffLL) return MLA_ERR_SHAPE;

@@ -163,14 +163,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t q_addr = smem_u32(smem + L.q_off), kv_addr = smem_u32(smem + L.kv_off), p_addr = smem_u32(p_s);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int g = blockIdx.y;
+    int s = blockIdx.x, b = blockIdx.z;
+    int bal_chunk = 0;
+    if (!FP8 && a.balanced) {
+        // one grid of split slots shared by all streams (every warp finds the same slot)
+        const BalancedPlan P = balanced_plan(a.seq_lens, a.B, a.q_len, a.slot_stride, a.bal_G);
+        balanced_slot(P, blockIdx.x, &b, &s);
+        if (b < 0) return;                               // slot beyond the streams' need: no work
+        bal_chunk = P.chunk;
+    }
     const int rows = a.q_len * a.H;
     const int row0 = g * R_step;
     const int nrows = min(R_step, rows - row0);
     const int n = FP8 ? a.slot_stride : a.seq_lens[b];
     const bool bad_len = FP8 ? false : (n < a.q_len || n > a.slot_stride);
     int k_begin = 0, k_end = 0;
-    if (!bad_len) split_range(n, a.nsplit, s, NK, &k_begin, &k_end);
+    if (!bad_len) {
+        if (!FP8 && a.balanced) {
+            k_begin = min(n, s * bal_chunk);
+            k_end = (int)min((long long)n, (long long)(s + 1) * bal_chunk);
+        } else {
+            split_range(n, a.nsplit, s, NK, &k_begin, &k_end);
+        }
+    }
+    // partial row of stream row rr: uniform [B * rows][nsplit] or balanced [slot][rows]
+    const int64_t part_row0 = (!FP8 && a.balanced) ? (int64_t)blockIdx.x * rows + row0
+                                                    : ((int64_t)b * rows + row0) * a.nsplit + s;
+    const int64_t part_row_step = (!FP8 && a.balanced) ? 1 : a.nsplit;
     // the swizzled layouts need a 1024-byte aligned base: otherwise report and do no work
     const bool misaligned = (smem_u32(smem) & 1023u) != 0;
     const int T = misaligned ? 0 : (k_end - k_begin + NK - 1) / NK;
@@ -533,7 +553,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int64_t grow0 = (int64_t)b * rows + row0;
         if (row_ok) {
             if (a.nsplit == 1) a.lse[grow0 + r] = lse_v;
-            else a.part_lse[(grow0 + r) * a.nsplit + s] = lse_v;
+            else a.part_lse[part_row0 + r * part_row_step] = lse_v;
         }
         bar_sync(2, 128);
         // O^T -> rows: thread = TMEM lane = value dim, each warp store writes 32 consecutive
@@ -555,7 +575,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int rr = c0 + jj;
                     if (rr < nrows) {
                         float* dst = a.nsplit == 1 ? a.out + (grow0 + rr) * D_V
-                                                   : a.part_out + ((grow0 + rr) * a.nsplit + s) * D_V;
+                                                   : a.part_out + (part_row0 + rr * part_row_step) * D_V;
                         dst[dim] = __uint_as_float(v[jj]) * M.rinv[rr];
                     }
                 }
@@ -619,7 +639,7 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
     if (!encode_bf16_2d_sw128(&q_map, a.q, D_QK, q_rows, D_QK * 2, 64, (uint32_t)R,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
         return cudaErrorInvalidValue;
-    dim3 grid(a.nsplit, n_tiles, a.B);
+    dim3 grid(a.nsplit, n_tiles, a.balanced ? 1 : a.B);
     int which;
     if (!a.kv_fp8) which = nq == 4 ? 0 : 1;
     else which = nq == 4 ? 2 : nq == 2 ? 3 : 4;

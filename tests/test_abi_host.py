@@ -92,11 +92,12 @@ def test_zero_streams_with_bad_pointers_is_ok(lib):
     assert _call_attn(lib, B=0, q=None, kv=None) == 0
 
 
-def test_partials_needs_explicit_nsplit(lib):
+def test_partials_split_count_range(lib):
     P = ctypes.c_void_p
-    rc = lib.mla_verify_partials(P(16), P(16), 10, P(16), 16, P(16), None, 1, 9, 8, 0.1, P(16), P(16), 0, None, 0,
-                                 None)
-    assert rc == -5
+    for ns in (-1, 1025):
+        rc = lib.mla_verify_partials(P(16), P(16), 10, P(16), 16, P(16), None, 1, 9, 8, 0.1, P(16), P(16), ns, None,
+                                     0, None)
+        assert rc == -5
 
 
 def test_fp8_argument_errors(lib):

@@ -47,18 +47,20 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // ---------------------------------------------------------------------------
-// Combine: one CTA of 256 threads per (row, 128 output dims).  Warp 0 turns the
-// row's S split log-sum-exps into the row's lse and the split weights
-// w_s = exp(lse_s - lse) (in shared memory); then thread (g, v), g = tid / 32,
-// v = tid % 32, sums float4 v of the 128 dims over splits s = g, g + 8, ... (many
-// independent 16-byte loads in flight), and the 8 group sums are added in shared
-// memory.  The launch may overlap the tail of the split kernel before it
-// (programmatic dependent launch); griddepcontrol.wait holds every thread until
+// Combine.  A work item is (row, 128 output dims); Z warps (Z = 1, 2, 4 or 8, more for
+// more splits) share an item, and a CTA of 8 warps holds 8 / Z items.  Lane v of warp
+// z sums float4 v of the item's dims over the splits s = z, z + Z, ... with weights
+// w_s = exp(lse_s - lse), lse = log sum_s exp(lse_s): the first eight partial loads of
+// a warp are issued before the weights are known, every warp derives the row's lse
+// from the S split values itself (no barrier before the sums), and the Z warp sums
+// meet in shared memory.  The launch may overlap the tail of the split kernel before
+// it (programmatic dependent launch); griddepcontrol.wait holds every thread until
 // that kernel has completed and its writes are visible.
 // ---------------------------------------------------------------------------
 constexpr int CB_THREADS = 256;
+constexpr int CB_WARPS = CB_THREADS / 32;
 constexpr int CB_DIMS = 128;
-constexpr int CB_GROUPS = CB_THREADS / 32;
+constexpr int CB_BATCH = 8;
 
 // Balanced partials (slot-major): the row's splits are slots first .. first + count - 1
 // of its stream, recomputed from the lengths exactly as the split kernel chose them.
@@ -68,21 +70,23 @@ struct CombineBalanced {
     int B, q_len, slot_stride, G, rows;
 };
 
+template <int Z>
 __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __restrict__ part_out,
-                                                             const float* __restrict__ part_lse, int S,
-                                                             float* __restrict__ out, float* __restrict__ lse,
-                                                             const CombineBalanced bal) {
-    extern __shared__ float wsm[];                  // [S] split weights
-    __shared__ float4 acc_s[CB_GROUPS][32];
-    __shared__ float row_stat[2];                   // lse, state (0 ok, 1 empty, 2 malformed)
+                                                             const float* __restrict__ part_lse, int S_all,
+                                                             long long n_items, float* __restrict__ out,
+                                                             float* __restrict__ lse, const CombineBalanced bal) {
+    __shared__ float4 red[CB_WARPS][32];
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int tid = threadIdx.x, lane = tid & 31, g = tid >> 5;
-    const long long row = blockIdx.x;
-    const int quarter = blockIdx.y;
-    // split s of this row: lse at pl[s * lse_step], output at po_row + s * out_step
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, z = warp % Z;
+    const long long item = (long long)blockIdx.x * (CB_WARPS / Z) + warp / Z;
+    const bool valid = item < n_items;
+    const long long row = valid ? item / (D_V / CB_DIMS) : 0;
+    const int quarter = (int)(item % (D_V / CB_DIMS));
+    // split s of this row: lse at pl[s * lse_step], output at part_out[po + s * out_step]
+    int S = S_all;
     long long lse_step = 1, out_step = D_V;
-    const float* pl = part_lse + row * S;
-    const float* po_row = part_out + row * (long long)S * D_V;
+    const float* pl = part_lse + row * S_all;
+    long long po = row * (long long)S_all * D_V;
     if (bal.on) {
         const BalancedPlan P = balanced_plan(bal.seq_lens, bal.B, bal.q_len, bal.slot_stride, bal.G);
         const int b = (int)(row / bal.rows), r = (int)(row % bal.rows);
@@ -92,74 +96,101 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __rest
         lse_step = bal.rows;
         out_step = (long long)bal.rows * D_V;
         pl = part_lse + (long long)first * bal.rows + r;
-        po_row = part_out + ((long long)first * bal.rows + r) * D_V;
+        po = ((long long)first * bal.rows + r) * D_V;
     }
+    if (!valid) S = 0;
+    const float* base = part_out + po + quarter * CB_DIMS + lane * 4;
 
-    if (g == 0) {
-        float mx = -INFINITY;
-        bool bad = false;
-        for (int s = lane; s < S; s += 32) {
-            const float v = pl[s * lse_step];
-            bad |= v != v;
-            mx = fmaxf(mx, v);
-        }
+    float4 v[CB_BATCH];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        bad = __any_sync(0xffffffffu, bad);
-        float z = 0.f;
-        if (!bad && mx != -INFINITY)
-            for (int s = lane; s < S; s += 32) z += expf(pl[s * lse_step] - mx);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        const float L = mx + logf(z);
-        for (int s = lane; s < S; s += 32) wsm[s] = (bad || mx == -INFINITY) ? 0.f : expf(pl[s * lse_step] - L);
-        if (lane == 0) {
-            row_stat[0] = bad ? __int_as_float(0x7fc00000) : (mx == -INFINITY ? -INFINITY : L);
-            row_stat[1] = bad ? 2.f : (mx == -INFINITY ? 1.f : 0.f);
-        }
+    for (int m = 0; m < CB_BATCH; ++m) {
+        const int s = z + Z * m;
+        if (s < S) v[m] = __ldg(reinterpret_cast<const float4*>(base + (long long)s * out_step));
     }
-    __syncthreads();
+    float mx = -INFINITY;
+    bool bad = false;
+    for (int s = lane; s < S; s += 32) {
+        const float x = __ldg(pl + s * lse_step);
+        bad |= x != x;
+        mx = fmaxf(mx, x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    bad = __any_sync(0xffffffffu, bad);
+    const bool live = !bad && mx != -INFINITY;
+    float zs = 0.f;
+    if (live)
+        for (int s = lane; s < S; s += 32) zs += expf(__ldg(pl + s * lse_step) - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
+    const float L = mx + logf(zs);
+
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row_stat[1] == 0.f) {
-        const float* base = po_row + quarter * CB_DIMS + lane * 4;
-#pragma unroll 4
-        for (int s = g; s < S; s += CB_GROUPS) {
-            const float w = wsm[s];
-            if (w == 0.f) continue;
-            const float4 v = *reinterpret_cast<const float4*>(base + (long long)s * out_step);
-            acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+    if (live) {
+        for (int s0 = 0; s0 < S; s0 += CB_BATCH * Z) {
+            if (s0 > 0) {
+#pragma unroll
+                for (int m = 0; m < CB_BATCH; ++m) {
+                    const int s = s0 + z + Z * m;
+                    if (s < S) v[m] = __ldg(reinterpret_cast<const float4*>(base + (long long)s * out_step));
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < CB_BATCH; ++m) {
+                const int s = s0 + z + Z * m;
+                if (s < S) {
+                    const float w = expf(__ldg(pl + s * lse_step) - L);
+                    acc.x += w * v[m].x; acc.y += w * v[m].y; acc.z += w * v[m].z; acc.w += w * v[m].w;
+                }
+            }
         }
     }
-    acc_s[g][lane] = acc;
-    __syncthreads();
-    if (g == 0) {
-        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (Z > 1) {
+        red[warp][lane] = acc;
+        __syncthreads();
+        if (z == 0)
 #pragma unroll
-        for (int k = 0; k < CB_GROUPS; ++k) {
-            const float4 v = acc_s[k][lane];
-            r.x += v.x; r.y += v.y; r.z += v.z; r.w += v.w;
-        }
-        reinterpret_cast<float4*>(out + row * D_V + quarter * CB_DIMS)[lane] = r;
-        if (quarter == 0 && lane == 0) lse[row] = row_stat[0];
+            for (int k = 1; k < Z; ++k) {
+                const float4 u = red[warp + k][lane];
+                acc.x += u.x; acc.y += u.y; acc.z += u.z; acc.w += u.w;
+            }
+    }
+    if (valid && z == 0) {
+        reinterpret_cast<float4*>(out + row * D_V + quarter * CB_DIMS)[lane] = acc;
+        if (quarter == 0 && lane == 0) lse[row] = bad ? __int_as_float(0x7fc00000) : (live ? L : -INFINITY);
     }
 }
 
-}  // namespace
-
-static cudaError_t launch_combine_any(const float* part_out, const float* part_lse, long long n_rows, int S,
-                                      float* out, float* lse, const CombineBalanced& bal, cudaStream_t stream) {
-    if (n_rows <= 0) return cudaSuccess;
+template <int Z>
+cudaError_t launch_combine_z(const float* part_out, const float* part_lse, long long n_rows, int S, float* out,
+                             float* lse, const CombineBalanced& bal, cudaStream_t stream) {
+    const long long items = n_rows * (D_V / CB_DIMS);
+    const long long per_cta = CB_WARPS / Z;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)n_rows, D_V / CB_DIMS);
+    cfg.gridDim = dim3((unsigned)((items + per_cta - 1) / per_cta));
     cfg.blockDim = dim3(CB_THREADS);
-    cfg.dynamicSmemBytes = (size_t)S * sizeof(float);
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, part_out, part_lse, S, out, lse, bal);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<Z>, part_out, part_lse, S, items, out, lse, bal);
+}
+
+}  // namespace
+
+// Z: warps per item, from the split count (up to 16 splits per warp, 8 warps at most;
+// balanced partials: a stream holds at most all slots, typically a few dozen: 4 warps).
+static cudaError_t launch_combine_any(const float* part_out, const float* part_lse, long long n_rows, int S,
+                                      float* out, float* lse, const CombineBalanced& bal, cudaStream_t stream) {
+    if (n_rows <= 0) return cudaSuccess;
+    const int per = bal.on ? 4 * 16 : S;
+    if (per <= 16) return launch_combine_z<1>(part_out, part_lse, n_rows, S, out, lse, bal, stream);
+    if (per <= 32) return launch_combine_z<2>(part_out, part_lse, n_rows, S, out, lse, bal, stream);
+    if (per <= 64) return launch_combine_z<4>(part_out, part_lse, n_rows, S, out, lse, bal, stream);
+    return launch_combine_z<8>(part_out, part_lse, n_rows, S, out, lse, bal, stream);
 }
 
 cudaError_t launch_combine(const float* part_out, const float* part_lse, long long n_rows, int S,

@@ -258,6 +258,15 @@ const char* mla_status_string(int status);
 /* Library ABI version (major * 100 + minor). */
 int mla_verify_version(void);
 
+/*
+ * Test hook for the failure-detection path: the next split-kernel launch (any entry
+ * point, any device) has its gather warps withhold their arrival on the first key
+ * tile, so the pipeline's bounded waits expire after about a second: the kernel sets
+ * MLA_DEV_TIMEOUT, writes zeros, releases its tensor memory and exits; no trap, no
+ * hang, and the context stays usable.  One-shot; returns MLA_OK.
+ */
+int mla_debug_stall_next_launch(void);
+
 #ifdef __cplusplus
 }
 #endif

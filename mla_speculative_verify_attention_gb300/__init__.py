@@ -33,7 +33,8 @@ DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
 EXPORTS = ("mla_verify_workspace_bytes", "mla_verify_auto_nsplit", "mla_verify_attn",
            "mla_verify_partials", "mla_verify_combine", "mla_verify_status",
            "mla_status_string", "mla_verify_version", "mla_verify_attn_static_scratch",
-           "mla_sparse_fp8_decode", "mla_sparse_fp8_partials", "mla_verify_attn_packed", "mla_kv_append")
+           "mla_sparse_fp8_decode", "mla_sparse_fp8_partials", "mla_verify_attn_packed", "mla_kv_append",
+           "mla_debug_stall_next_launch")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
@@ -84,6 +85,8 @@ def load():
     L.mla_status_string.restype = ctypes.c_char_p
     L.mla_verify_version.argtypes = []
     L.mla_verify_version.restype = I
+    L.mla_debug_stall_next_launch.argtypes = []
+    L.mla_debug_stall_next_launch.restype = I
     _lib = L
     return L
 

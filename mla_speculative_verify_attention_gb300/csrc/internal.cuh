@@ -39,6 +39,9 @@ struct VerifyArgs {
     // part_out [nsplit][q_len * H][512], part_lse [nsplit][q_len * H]
     int balanced;
     int bal_G;
+    // test hook (mla_debug_stall_next_launch): the gather warps withhold their arrival on
+    // key tile 0, so the pipeline's bounded waits expire and report DEV_TIMEOUT
+    int debug_stall;
     // fp8 sparse decode (kv_fp8 != 0): keys come from per-stream index lists
     // (slot = topk_slots [B, slot_stride = topk], seq_lens unused, q_len = 1) and
     // each key row is an e4m3 latent [512] with a per-token fp32 scale plus a bf16
@@ -139,6 +142,9 @@ __device__ inline void balanced_stream(const BalancedPlan& P, int b, int* first,
 }
 
 constexpr int BALANCED_MAX_STREAMS = 64;
+
+// One-shot test hook, consumed by the next split-kernel launch on any device.
+bool take_debug_stall();
 
 // Launchers (each returns the cudaError_t of the launch).
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);

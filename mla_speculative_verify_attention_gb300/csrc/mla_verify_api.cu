@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "../../include/mla_verify.h"
 #include "internal.cuh"
 
@@ -12,6 +14,10 @@ namespace mla {
 
 // Per-device status word of MLA_DEV_* bits (sticky until mla_verify_status clears it).
 __device__ unsigned g_status;
+
+// Test hook: the next split-kernel launch withholds its first key-tile arrival.
+static std::atomic<bool> g_debug_stall{false};
+bool take_debug_stall() { return g_debug_stall.exchange(false); }
 
 namespace {
 
@@ -480,5 +486,10 @@ const char* mla_status_string(int status) {
 }
 
 int mla_verify_version(void) { return 100; }
+
+int mla_debug_stall_next_launch(void) {
+    g_debug_stall.store(true);
+    return MLA_OK;
+}
 
 }  // extern "C"

@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t dst = base + (pc >> 3) * REGION + key * 128 + (((pc & 7) ^ (key & 7)) << 4);
                     cp_async16(dst, a.kv + (int64_t)row_slot * D_QK + pc * 8);
                 }
-                cp_async_arrive_noinc(&M.bars[B_KV_FULL + st]);
+                if (!(a.debug_stall && i == 0)) cp_async_arrive_noinc(&M.bars[B_KV_FULL + st]);
             } else {
                 // latent: row it of the warp's 8, lane = 16 e4m3 codes (dims 16 lane .. 16 lane + 15);
                 // rope: 8 rows x 8 pieces of 16 bytes, two per lane.  All loads first, then
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     *reinterpret_cast<uint4*>(sbase + 8 * REGION + key * 128 + ((c ^ (key & 7)) << 4)) = rope[it];
                 }
                 fence_proxy_async_smem();              // generic stores -> tensor-core reads
-                mbar_arrive(&M.bars[B_KV_FULL + st]);
+                if (!(a.debug_stall && i == 0)) mbar_arrive(&M.bars[B_KV_FULL + st]);
             }
         }
         cp_async_wait_all();
@@ -622,7 +622,9 @@ cudaError_t launch_one(bool set_attr, dim3 grid, cudaStream_t stream, const Veri
 }
 }  // namespace
 
-cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
+cudaError_t launch_verify_tc(const VerifyArgs& a_in, cudaStream_t stream) {
+    VerifyArgs a = a_in;
+    a.debug_stall = take_debug_stall() ? 1 : 0;
     static bool attr_set[64][5];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

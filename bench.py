@@ -400,6 +400,11 @@ def run_gpu(args):
     ws = torch.empty(max(mv.workspace_bytes(B, q_len, H, ns), 256), dtype=torch.uint8, device=dev)
     call_ns = args.nsplit
     split_desc = f"uniform, {ns} per stream"
+    if call_ns == 0 and isinstance(wl, Fp8Workload):
+        # the fp8 call's automatic count: one wave (equal-length streams), >= 128 keys per split
+        tiles = -(-H // 80)
+        ns = max(1, min(mv.num_sms(dev) // (B * tiles), -(-wl.max_seq // 128)))
+        split_desc = f"uniform, {ns} per stream (one wave)"
     if call_ns == 0 and not isinstance(wl, Fp8Workload) and 2 <= B <= 64:
         tiles = -(-(q_len * H) // 96)
         slots = mv.num_sms(dev) // tiles

@@ -202,7 +202,10 @@ int mla_verify_combine(const float* part_out, const float* part_lse, int B, int 
  *   kv_rope    bf16 [n_pool, 64], 16-byte aligned
  *   topk_slots int32 [B, topk], pool rows (any order; duplicates count twice)
  *   out fp32 [B, H, 512], lse fp32 [B, H]; nsplit / workspace as for mla_verify_attn
- *   (mla_verify_workspace_bytes(B, 1, H, nsplit)).
+ *   (mla_verify_workspace_bytes(B, 1, H, nsplit)).  nsplit = 0: every stream has the
+ *   same topk keys, so the automatic count fills one wave of CTAs, min(SMs / (B x row
+ *   tiles), ceil(topk / 128)) splits per stream (a workspace sized for
+ *   mla_verify_auto_nsplit(B, 1, H, topk, SMs, ...) always holds it).
  * Limits: 1 <= H <= 128, 0 <= B <= 65535, topk >= 1, 1 <= n_pool <= 2^31 - 1.
  * An index outside [0, n_pool) sets MLA_DEV_BAD_SLOT and reads pool row 0.
  */

@@ -41,6 +41,8 @@ def lib():
         L.oracle_mla_verify_packed.restype = I32
         L.oracle_kv_append.argtypes = [P, I64, P, I32, P, P, I32, I32]
         L.oracle_kv_append.restype = I32
+        L.oracle_kv_append_rows.argtypes = [P, I64, I64, P, P, I64]
+        L.oracle_kv_append_rows.restype = I32
         L.oracle_mla_combine.argtypes = [P, P, I64, I32, I32, P, P]
         L.oracle_mla_combine.restype = None
         L.oracle_mla_sparse_fp8.argtypes = [P, P, P, P, I64, P, I32, I32, I32, D, P, I64, P, P, I32]
@@ -136,6 +138,23 @@ def kv_append(kv_bits, slot_table, seq_lens, new_kv_bits):
     if rc != 0:
         raise ValueError(f"oracle_kv_append failed with status {rc}")
     return kv
+
+
+def kv_append_fp8(kv_lat, kv_scale, kv_rope_bits, slots, new_lat, new_scale, new_rope_bits):
+    """fp8 cache append: copies of (kv_lat [n_pool, 512] u8, kv_scale [n_pool] f32, kv_rope
+    [n_pool, 64] u16 bf16 bits) with row i of the new arrays written to pool row slots[i]."""
+    out = []
+    sl = _c(slots, np.int32)
+    for cache, new in ((kv_lat, new_lat), (kv_scale, new_scale), (kv_rope_bits, new_rope_bits)):
+        c = np.array(cache, copy=True, order="C")
+        n = np.ascontiguousarray(new, dtype=c.dtype)
+        row_bytes = c.itemsize * (c.shape[1] if c.ndim == 2 else 1)
+        assert n.shape[0] == sl.size and n.size * n.itemsize == sl.size * row_bytes
+        rc = lib().oracle_kv_append_rows(_ptr(c), c.shape[0], row_bytes, _ptr(sl), _ptr(n), sl.size)
+        if rc != 0:
+            raise ValueError(f"oracle_kv_append_rows failed with status {rc}")
+        out.append(c)
+    return tuple(out)
 
 
 def combine(part_out, part_lse):

@@ -379,3 +379,19 @@ int oracle_mla_sparse_fp8(const uint16_t* q, const uint8_t* kv_lat, const float*
     S.topk_slots = topk_slots; S.topk = topk; S.B = B; S.H = H;
     return run_jobs(&S.base, nthreads, sparse_worker, sizeof(sparse_job));
 }
+
+/*
+ * Row scatter of the fp8 cache's append: row i of each source array goes to pool row
+ * slots[i] of the matching cache array (latent codes, per-token scale, rope), the rows
+ * having been quantised by the caller (the pages fix no quantisation rule).  All
+ * slots are checked first; on an error nothing is written.
+ */
+int oracle_kv_append_rows(uint8_t* dst, int64_t n_pool, int64_t row_bytes, const int32_t* slots,
+                          const uint8_t* src, int64_t n_rows) {
+    if (!dst || !slots || !src || n_rows < 0 || row_bytes < 1) return OR_ERR_ARG;
+    for (int64_t i = 0; i < n_rows; ++i)
+        if (slots[i] < 0 || slots[i] >= n_pool) return OR_ERR_SLOT;
+    for (int64_t i = 0; i < n_rows; ++i)
+        memcpy(dst + (int64_t)slots[i] * row_bytes, src + i * row_bytes, (size_t)row_bytes);
+    return OR_OK;
+}

@@ -435,3 +435,19 @@ def test_kv_append_rejects_bad_slot_or_length():
         oracle.kv_append(inp.kv_bits, st, inp.seq_lens, drafts)
     with pytest.raises(ValueError):
         oracle.kv_append(inp.kv_bits, inp.slot_table, np.array([3], np.int32), drafts)
+
+
+def test_fp8_append_row_scatter_against_numpy_indexing():
+    f = w.make_sparse_fp8("app8", 3, 4, 16, 64, seed=47)
+    rng = np.random.default_rng(5)
+    slots = rng.permutation(f.n_pool)[:5].astype(np.int32)
+    new_lat = rng.integers(0, 256, (5, 512), dtype=np.uint8)
+    new_sc = rng.uniform(0.5, 2.0, 5).astype(np.float32)
+    new_rope = rng.integers(0, 1 << 16, (5, 64), dtype=np.uint16)
+    lat, sc, rope = oracle.kv_append_fp8(f.kv_lat, f.kv_scale, f.kv_rope, slots, new_lat, new_sc, new_rope)
+    e_lat, e_sc, e_rope = f.kv_lat.copy(), f.kv_scale.copy(), f.kv_rope.copy()
+    e_lat[slots], e_sc[slots], e_rope[slots] = new_lat, new_sc, new_rope
+    assert np.array_equal(lat, e_lat) and np.array_equal(sc, e_sc) and np.array_equal(rope, e_rope)
+    with pytest.raises(ValueError):
+        oracle.kv_append_fp8(f.kv_lat, f.kv_scale, f.kv_rope, np.array([f.n_pool], np.int32), new_lat[:1],
+                             new_sc[:1], new_rope[:1])

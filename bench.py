@@ -339,21 +339,28 @@ class Fp8Workload:
                                   lse=lse.view(self.B, self.H), nsplit=ns, workspace=ws, stream=stream)
 
     def host_inputs(self):
-        """Queries, top-k lists and the one new token row per stream (latent, scale, rope)."""
+        """Queries, top-k lists and the one new token row per stream (latent codes, scale,
+        rope; staged contiguously and written into the pool by the fp8 append kernel)."""
         import torch
         f = self.f
         pairs = [(torch.from_numpy(f.q_bits.view(np.int16)).pin_memory(), self.q.view(torch.int16)),
                  (torch.from_numpy(np.ascontiguousarray(f.topk_slots)).pin_memory(), self.ts)]
-        for b in range(f.B):
-            r = int(f.topk_slots[b, 0])
-            pairs.append((torch.from_numpy(f.kv_lat[r:r + 1].copy()).pin_memory(), self.lat[r:r + 1]))
-            pairs.append((torch.from_numpy(f.kv_scale[r:r + 1].copy()).pin_memory(), self.sc[r:r + 1]))
-            pairs.append((torch.from_numpy(f.kv_rope[r:r + 1].view(np.int16).copy()).pin_memory(),
-                          self.rope.view(torch.int16)[r:r + 1]))
+        rows = np.ascontiguousarray(f.topk_slots[:, 0])
+        self.new_slots = torch.empty(rows.shape, dtype=torch.int32, device=self.dev)
+        self.new_lat = torch.empty((f.B, 512), dtype=torch.uint8, device=self.dev)
+        self.new_sc = torch.empty((f.B,), dtype=torch.float32, device=self.dev)
+        self.new_rope = torch.empty((f.B, 64), dtype=torch.bfloat16, device=self.dev)
+        pairs += [(torch.from_numpy(rows).pin_memory(), self.new_slots),
+                  (torch.from_numpy(f.kv_lat[rows].copy()).pin_memory(), self.new_lat),
+                  (torch.from_numpy(f.kv_scale[rows].copy()).pin_memory(), self.new_sc),
+                  (torch.from_numpy(f.kv_rope[rows].view(np.int16).copy()).pin_memory(), self.new_rope.view(torch.int16))]
         return pairs
 
     def before_call(self, stream):
-        return 0
+        """fp8 KV append of the staged new rows (end-to-end step only); returns launches."""
+        self.mv.kv_append_fp8(self.lat, self.sc, self.rope, self.new_slots, self.new_lat, self.new_sc, self.new_rope,
+                              stream=stream)
+        return 1
 
     def oracle_call(self, threads):
         import oracle

@@ -154,6 +154,21 @@ int mla_kv_append(void* kv_cache, int64_t n_pool, const int32_t* slot_table, int
                   const int32_t* seq_lens, const void* new_kv, int B, int q_len, mla_stream_t stream);
 
 /*
+ * KV append for the fp8 cache of mla_sparse_fp8_decode(): row i of the new arrays
+ * goes to pool row slots[i] of each cache array.  The rows arrive quantised (e4m3
+ * codes and their per-token scale, as the cache holds them; the pages fix no
+ * quantisation rule), so this is a plain scatter.
+ *   kv_lat uint8 [n_pool, 512], kv_scale fp32 [n_pool], kv_rope bf16 [n_pool, 64]: written
+ *   slots int32 [n_rows]; new_lat uint8 [n_rows, 512]; new_scale fp32 [n_rows];
+ *   new_rope bf16 [n_rows, 64]; lat / rope arrays 16-byte aligned
+ * Slots of one call must be distinct.  A slot outside [0, n_pool) skips that row and
+ * sets MLA_DEV_BAD_SLOT.  n_rows == 0 is a no-op.
+ */
+int mla_kv_append_fp8(uint8_t* kv_lat, float* kv_scale, void* kv_rope, int64_t n_pool, const int32_t* slots,
+                      const uint8_t* new_lat, const float* new_scale, const void* new_rope, int n_rows,
+                      mla_stream_t stream);
+
+/*
  * The split stage of mla_verify_attn() alone: with nsplit >= 2 it writes the
  * partial outputs and log-sum-exps into `workspace` (layout of
  * mla_verify_workspace_bytes) and enqueues nothing else; nsplit must be given

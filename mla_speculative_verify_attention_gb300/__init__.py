@@ -33,7 +33,7 @@ DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
 EXPORTS = ("mla_verify_workspace_bytes", "mla_verify_auto_nsplit", "mla_verify_attn",
            "mla_verify_partials", "mla_verify_combine", "mla_verify_status",
            "mla_status_string", "mla_verify_version", "mla_verify_attn_static_scratch",
-           "mla_sparse_fp8_decode", "mla_sparse_fp8_partials", "mla_verify_attn_packed", "mla_kv_append",
+           "mla_sparse_fp8_decode", "mla_sparse_fp8_partials", "mla_verify_attn_packed", "mla_kv_append", "mla_kv_append_fp8",
            "mla_debug_stall_next_launch")
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -77,6 +77,8 @@ def load():
     L.mla_verify_attn_static_scratch.restype = I
     L.mla_kv_append.argtypes = [P, I64, P, I, P, P, I, I, P]
     L.mla_kv_append.restype = I
+    L.mla_kv_append_fp8.argtypes = [P, P, P, I64, P, P, P, P, I, P]
+    L.mla_kv_append_fp8.restype = I
     L.mla_verify_combine.argtypes = [P, P, I, I, I, I, P, P, P]
     L.mla_verify_combine.restype = I
     L.mla_verify_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I]
@@ -190,6 +192,26 @@ def kv_append(kv_cache: torch.Tensor, slot_table: torch.Tensor, seq_lens: torch.
                          _ptr(new_kv), B, q_len, _stream(stream))
     _check("mla_kv_append", rc)
     return kv_cache
+
+
+def kv_append_fp8(kv_lat, kv_scale, kv_rope, slots, new_lat, new_scale, new_rope, stream=None):
+    """mla_kv_append_fp8: quantised rows (new_lat [n, 512] u8, new_scale [n] f32, new_rope [n, 64]
+    bf16) into the fp8 cache at pool rows slots [n] (int32)."""
+    L = load()
+    if kv_lat.dtype != torch.uint8 or new_lat.dtype != torch.uint8 or kv_scale.dtype != torch.float32 or \
+            new_scale.dtype != torch.float32 or kv_rope.dtype != torch.bfloat16 or new_rope.dtype != torch.bfloat16:
+        raise TypeError("kv_lat/new_lat uint8, kv_scale/new_scale float32, kv_rope/new_rope bfloat16")
+    if slots.dtype != torch.int32:
+        raise TypeError("slots must be int32")
+    for t in (kv_lat, kv_scale, kv_rope, slots, new_lat, new_scale, new_rope):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    n = slots.numel()
+    if new_lat.shape != (n, D_V) or new_scale.shape != (n,) or new_rope.shape != (n, 64):
+        raise ValueError("new rows must be [n, 512], [n], [n, 64] for n slots")
+    rc = L.mla_kv_append_fp8(_ptr(kv_lat), _ptr(kv_scale), _ptr(kv_rope), kv_lat.shape[0], _ptr(slots),
+                             _ptr(new_lat), _ptr(new_scale), _ptr(new_rope), n, _stream(stream))
+    _check("mla_kv_append_fp8", rc)
 
 
 def verify_attn_static_scratch(q: torch.Tensor, kv_cache: torch.Tensor, slot_table: torch.Tensor,

@@ -155,6 +155,9 @@ constexpr int TC_MAX_ROWS = 96;
 cudaError_t launch_kv_append(__nv_bfloat16* kv, const int32_t* slot, int slot_stride, const int32_t* seq_lens,
                              const __nv_bfloat16* new_kv, int B, int q_len, int64_t n_pool, unsigned* status,
                              cudaStream_t stream);
+cudaError_t launch_kv_append_fp8(uint8_t* kv_lat, float* kv_scale, __nv_bfloat16* kv_rope, int64_t n_pool,
+                                 const int32_t* slots, const uint8_t* new_lat, const float* new_scale,
+                                 const __nv_bfloat16* new_rope, int n_rows, unsigned* status, cudaStream_t stream);
 cudaError_t launch_combine(const float* part_out, const float* part_lse, long long n_rows, int S,
                            float* out, float* lse, cudaStream_t stream);
 // Combine of a balanced split (slot-major partials of VerifyArgs::balanced).

@@ -36,7 +36,40 @@ __global__ void __launch_bounds__(APPEND_THREADS)
     for (int k = lane; k < D_QK / 8; k += 32) dst[k] = __ldg(src + k);
 }
 
+// fp8 cache: one warp per appended row; lanes 0-31 copy the 512 code bytes, lanes 0-7
+// the 128 rope bytes, lane 0 the scale.  The rows arrive quantised.
+__global__ void __launch_bounds__(APPEND_THREADS)
+    kv_append_fp8_kernel(uint8_t* __restrict__ kv_lat, float* __restrict__ kv_scale,
+                         __nv_bfloat16* __restrict__ kv_rope, int64_t n_pool, const int32_t* __restrict__ slots,
+                         const uint8_t* __restrict__ new_lat, const float* __restrict__ new_scale,
+                         const __nv_bfloat16* __restrict__ new_rope, int n_rows, unsigned* status) {
+    const long long i = ((long long)blockIdx.x * APPEND_THREADS + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (i >= n_rows) return;
+    const int s = slots[i];
+    if (s < 0 || (int64_t)s >= n_pool) {
+        if (lane == 0) atomicOr(status, DEV_BAD_SLOT);
+        return;
+    }
+    reinterpret_cast<uint4*>(kv_lat + (int64_t)s * D_V)[lane] =
+        __ldg(reinterpret_cast<const uint4*>(new_lat + i * D_V) + lane);
+    if (lane < 8)
+        reinterpret_cast<uint4*>(kv_rope + (int64_t)s * 64)[lane] =
+            __ldg(reinterpret_cast<const uint4*>(new_rope + i * 64) + lane);
+    if (lane == 0) kv_scale[s] = __ldg(new_scale + i);
+}
+
 }  // namespace
+
+cudaError_t launch_kv_append_fp8(uint8_t* kv_lat, float* kv_scale, __nv_bfloat16* kv_rope, int64_t n_pool,
+                                 const int32_t* slots, const uint8_t* new_lat, const float* new_scale,
+                                 const __nv_bfloat16* new_rope, int n_rows, unsigned* status, cudaStream_t stream) {
+    const long long threads = (long long)n_rows * 32;
+    const unsigned blocks = (unsigned)((threads + APPEND_THREADS - 1) / APPEND_THREADS);
+    kv_append_fp8_kernel<<<blocks, APPEND_THREADS, 0, stream>>>(kv_lat, kv_scale, kv_rope, n_pool, slots, new_lat,
+                                                                 new_scale, new_rope, n_rows, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_kv_append(__nv_bfloat16* kv, const int32_t* slot, int slot_stride, const int32_t* seq_lens,
                              const __nv_bfloat16* new_kv, int B, int q_len, int64_t n_pool, unsigned* status,

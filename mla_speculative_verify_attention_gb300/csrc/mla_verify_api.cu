@@ -452,6 +452,26 @@ int mla_verify_partials(const void* q, const void* kv_cache, int64_t n_pool, con
                       H, scale, out, lse, nsplit, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int mla_kv_append_fp8(uint8_t* kv_lat, float* kv_scale, void* kv_rope, int64_t n_pool, const int32_t* slots,
+                      const uint8_t* new_lat, const float* new_scale, const void* new_rope, int n_rows,
+                      mla_stream_t stream) {
+    if (n_rows < 0) return MLA_ERR_SHAPE;
+    if (n_rows == 0) return MLA_OK;
+    if (!kv_lat || !kv_scale || !kv_rope || !slots || !new_lat || !new_scale || !new_rope) return MLA_ERR_NULL;
+    if (n_pool < 1 || n_pool > 0x7fffffffLL) return MLA_ERR_SHAPE;
+    if (!aligned(kv_lat, 16) || !aligned(new_lat, 16) || !aligned(kv_rope, 16) || !aligned(new_rope, 16) ||
+        !aligned(kv_scale, 4) || !aligned(new_scale, 4) || !aligned(slots, 4))
+        return MLA_ERR_ALIGN;
+    unsigned* status = nullptr;
+    int rc = device_state(nullptr, &status, nullptr);
+    if (rc != MLA_OK) return rc;
+    if (launch_kv_append_fp8(kv_lat, kv_scale, static_cast<__nv_bfloat16*>(kv_rope), n_pool, slots, new_lat,
+                             new_scale, static_cast<const __nv_bfloat16*>(new_rope), n_rows, status,
+                             reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MLA_ERR_LAUNCH;
+    return MLA_OK;
+}
+
 int mla_verify_combine(const float* part_out, const float* part_lse, int B, int q_len, int H, int S, float* out,
                        float* lse, mla_stream_t stream) {
     if (B < 0 || q_len < 1 || H < 1 || (long long)B * q_len * H > 0x7fffffffLL) return MLA_ERR_SHAPE;

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import workloads as w
-from gpu_util import compare
+from gpu_util import bf16, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -69,3 +69,35 @@ def test_bad_index_sets_status_without_faulting(cuda_lib):
     assert mv.device_status(clear=True) & mv.DEV_BAD_SLOT
     ro, rl = oracle.sparse_fp8(f.q_bits[:1], f.kv_lat, f.kv_scale, f.kv_rope, f.topk_slots[:1], f.scale)
     compare(out[:1], lse[:1], ro, rl, what="good stream next to a bad index")
+
+
+def test_fp8_append_then_decode(cuda_lib):
+    """mla_kv_append_fp8 writes quantised rows bit-exactly (against the oracle's scatter);
+    the decode that follows reads them."""
+    mv = cuda_lib
+    f = w.make_sparse_fp8("app8", 4, 16, 300, 1024, seed=99)
+    rows = np.ascontiguousarray(f.topk_slots[:, 0]).astype(np.int32)
+    noisy_lat = f.kv_lat.copy()
+    noisy_sc = f.kv_scale.copy()
+    noisy_rope = f.kv_rope.copy()
+    rng = np.random.default_rng(3)
+    noisy_lat[rows] = rng.integers(0, 127, (rows.size, 512), dtype=np.uint8)
+    noisy_sc[rows] = 7.0
+    noisy_rope[rows] = 0
+    e_lat, e_sc, e_rope = oracle.kv_append_fp8(noisy_lat, noisy_sc, noisy_rope, rows, f.kv_lat[rows],
+                                               f.kv_scale[rows], f.kv_rope[rows])
+    lat = torch.from_numpy(noisy_lat).cuda()
+    sc = torch.from_numpy(noisy_sc).cuda()
+    rope = torch.from_numpy(noisy_rope.view(np.int16)).cuda().view(torch.bfloat16)
+    mv.kv_append_fp8(lat, sc, rope, torch.from_numpy(rows).cuda(), torch.from_numpy(f.kv_lat[rows].copy()).cuda(),
+                     torch.from_numpy(f.kv_scale[rows].copy()).cuda(),
+                     torch.from_numpy(f.kv_rope[rows].view(np.int16).copy()).cuda().view(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert np.array_equal(lat.cpu().numpy(), e_lat) and np.array_equal(sc.cpu().numpy(), e_sc)
+    assert np.array_equal(rope.view(torch.int16).cpu().numpy().view(np.uint16), e_rope)
+    q = bf16(f.q_bits)
+    out, lse = mv.sparse_fp8_decode(q, lat, sc, rope, torch.from_numpy(f.topk_slots).cuda(), f.scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.sparse_fp8_inputs(f)
+    compare(out, lse, ro, rl, what="fp8 append + decode")
+    assert mv.device_status() == 0

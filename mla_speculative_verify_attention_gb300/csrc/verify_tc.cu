@@ -29,9 +29,10 @@
 // and the M-major A operand of V^T P^T (V = first 512 dims of each key row).
 //
 // Warp roles (320 threads):
-//   warp 0      TMEM allocation; runs the MMA issue loop as a whole warp (operands
-//               stay warp-uniform) and one elected lane issues every MMA and commit
-//   warp 1      TMA copies of the shared-memory part of the Q tile (64-dim boxes of R rows)
+//   warp 0      TMEM allocation; Q K^T issue loop run by the whole warp (operands stay
+//               warp-uniform), one elected lane issuing each MMA and commit (fp8: P V too)
+//   warp 1      TMA copies of the shared-memory part of the Q tile (64-dim boxes of R
+//               rows), then (bf16) the P V issue loop in the same style
 //   warps 2-5   Q chunks into TMEM (thread = query row), softmax (thread = query row =
 //               TMEM lane) and the epilogue (thread = value dim = TMEM lane of O^T);
 //               TMEM lane quadrant = warp % 4
@@ -224,8 +225,98 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *M.tmem_slot;
 
-    if (warp == 0) {
-        // ================= MMA issuer (lane 0) =================
+    if (!FP8 && warp <= 1) {
+        // ================= MMA issue, bf16: warp 0 Q K^T, warp 1 P V =================
+        // Two issuers: Q K^T of tile i goes out as soon as its keys and S buffer are ready,
+        // P V of tile j as soon as its P is written, so a key stage is released right after
+        // its P V instead of after the next tile's Q K^T (measured on GB300: c4 -7%,
+        // c3-64k -5%).  They write different TMEM columns (S buffers / O^T) and only read
+        // shared memory; each commit tracks its own thread's MMAs.  The fp8 path keeps one
+        // issuer (P V of tile i - 1 after Q K^T of tile i): split issue measured slower there.
+        if (warp == 1 && T > 0 && lane == 0) {
+            // the Q tile copies come first
+            mbar_arrive_expect_tx(&M.bars[B_Q_FULL], (uint32_t)(nq_s * R * 128));
+            const int qrow = b * rows + row0;
+            for (int c = nq_t; c < NCHUNK; ++c)
+                tma_load_2d(q_addr + (c - nq_t) * R * 128, &q_map, c * 64, qrow, &M.bars[B_Q_FULL]);
+        }
+        __syncwarp();
+        if (T > 0) {
+            const uint32_t id_qk = idesc_bf16(128, NK, false, false);
+            const uint32_t id_pv = idesc_bf16(128, R, true, false);
+            // Q (shared-memory chunks): K-major, 128-byte swizzle, 8-row groups 1024 B apart;
+            // a 16-dim step moves 32 B inside the 128-byte rows, a 64-dim step moves to the
+            // next region (R * 128 B)
+            const uint64_t dq = smem_desc_sw128(q_addr, 16, 1024);
+            // key stage: the same layout with 32-row regions (REGION bytes)
+            const uint64_t dk = smem_desc_sw128(kv_addr, 16, 1024);
+            // V^T: M-major, 64-dim chunks REGION apart, 8-key groups 1024 B apart
+            const uint64_t dv = smem_desc_sw128(kv_addr, REGION, 1024);
+            // P: K-major, no swizzle, 8-key blocks R * 16 B apart, 8-row blocks 128 B apart
+            const uint64_t dp = smem_desc(p_addr, R * 16, 128);
+            const uint32_t q_region16 = (uint32_t)(R * 128) >> 4;
+            bool ok = true;
+            if (warp == 1) {
+                for (int j = 0; j < T && ok; ++j) {
+                    ok = mbar_wait(&M.bars[B_P_FULL + (j & 1)], (j >> 1) & 1, M.abort);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t st16 = (uint64_t)((j % STAGES) * STAGE_BYTES) >> 4;
+                    if (elect_one()) {
+#pragma unroll
+                    for (int ci = 0; ci < 4; ++ci)
+#pragma unroll
+                        for (int kk = 0; kk < NK / 16; ++kk)
+                            mma_bf16(tmem + O_COL0 + ci * R,
+                                     dv + st16 + (uint64_t)((2 * ci * REGION + kk * 2048) >> 4),
+                                     dp + (uint64_t)(((j & 1) * R * NK * 2 + kk * 2 * R * 16) >> 4), id_pv,
+                                     j > 0 || kk > 0);
+                    mma_commit(&M.bars[B_KV_EMPTY + j % STAGES]);
+                    }
+                    __syncwarp();
+                }
+            } else {
+                ok = mbar_wait(&M.bars[B_Q_FULL], 0, M.abort);
+                ok = ok && mbar_wait(&M.bars[B_QT_FULL], 0, M.abort);
+                ok = __all_sync(0xffffffffu, ok);
+                for (int i = 0; i < T && ok; ++i) {
+                    const int st = i % STAGES;
+                    ok = mbar_wait(&M.bars[B_KV_FULL + st], (i / STAGES) & 1, M.abort);
+                    if (ok && i >= 2) ok = mbar_wait(&M.bars[B_S_FREE + (i & 1)], ((i - 2) >> 1) & 1, M.abort);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    fence_proxy_async_smem();          // cp.async (generic proxy) data -> tensor-core reads
+                    tc_fence_after();
+                    const uint64_t st16 = (uint64_t)(st * STAGE_BYTES) >> 4;
+                    const uint32_t d_s = tmem + (i & 1) * SC;
+                    if (elect_one()) {
+#pragma unroll
+                    for (int ks = 0; ks < D_QK / 16; ++ks) {
+                        const int c = ks >> 2;
+                        const uint32_t ko = (uint32_t)((c * REGION + (ks & 3) * 32) >> 4);
+                        // fp8 path: latent dims (ks < 32) and rope dims accumulate separately, so
+                        // the per-key scale can multiply the latent part alone
+                        const bool rope = FP8 && ks >= D_V / 16;
+                        const uint32_t d = rope ? d_s + NK : d_s;
+                        const bool acc = rope ? ks > D_V / 16 : ks > 0;
+                        if (c < nq_t) {
+                            mma_bf16_ta(d, tmem + Q_COL0 + ks * 8, dk + st16 + ko, id_qk, acc);
+                        } else {
+                            const uint32_t qo = (uint32_t)(c - nq_t) * q_region16 + (uint32_t)(ks & 3) * 2;
+                            mma_bf16(d, dq + qo, dk + st16 + ko, id_qk, acc);
+                        }
+                    }
+                    mma_commit(&M.bars[B_S_FULL + (i & 1)]);
+                    }
+                    __syncwarp();
+                }
+            }
+            if (!ok && lane == 0) give_up(M, a.status);
+        }
+        __syncwarp();
+    } else if (FP8 && warp == 0) {
+        // ================= MMA issue, fp8: warp 0 issues Q K^T and P V =================
         if (T > 0) {
             const uint32_t id_qk = idesc_bf16(128, NK, false, false);
             const uint32_t id_pv = idesc_bf16(128, R, true, false);
@@ -298,7 +389,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!ok && lane == 0) give_up(M, a.status);
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (FP8 && warp == 1) {
         // ================= Q tile copies =================
         if (T > 0 && lane == 0) {
             mbar_arrive_expect_tx(&M.bars[B_Q_FULL], (uint32_t)(nq_s * R * 128));

@@ -42,6 +42,7 @@
 // gather sized to the SM's load path, and the split-count policy of the host code.
 #include <cuda_fp8.h>
 
+#include "fp8_decode.cuh"
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -58,6 +59,11 @@ constexpr int GATHER_WARPS = 4;
 constexpr int NCHUNK = D_QK / 64;                    // 9 swizzled 64-dim regions per row
 constexpr int REGION = NK * 128;                     // one 64-dim region of a stage: 4096 B
 constexpr int STAGE_BYTES = NCHUNK * REGION;         // 36864 B
+// fp8 path: raw slot of one key tile as read from memory, before widening to bf16
+constexpr int RAW_ROPE = NK * D_V;                   // e4m3 latents [NK][512], then
+constexpr int RAW_SCALE = RAW_ROPE + NK * 128;       // bf16 ropes [NK][64], then
+constexpr int RAW_SLOT = RAW_SCALE + NK * 4;         // fp32 scales [NK]: 20608 B
+constexpr int MAX_RAW_SLOTS = 4;
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns: S buffers first (bf16 path: two of 32 columns; fp8 path: two pairs
 // of latent / rope scores), then O^T
@@ -73,7 +79,7 @@ template <int STAGES> struct Bars {
                          P_FULL = 2 * STAGES + 4, Q_FULL = 2 * STAGES + 6, QT_FULL = 2 * STAGES + 7,
                          COUNT = 2 * STAGES + 8;    // P_FULL: one per P buffer
 };
-static_assert(Bars<3>::COUNT * 8 <= 128 && Bars<4>::COUNT * 8 <= 128, "barrier area");
+static_assert(Bars<2>::COUNT * 8 <= 128 && Bars<3>::COUNT * 8 <= 128 && Bars<4>::COUNT * 8 <= 128, "barrier area");
 
 struct Layout {
     int q_off, kv_off, p_off, misc_off, total;
@@ -126,29 +132,10 @@ __device__ __forceinline__ void give_up(const Misc& m, unsigned* status) {
     if (atomicExch(const_cast<int*>(m.abort), 1) == 0) atomicOr(status, DEV_TIMEOUT);
 }
 
-// Sixteen e4m3 codes -> sixteen bf16 values (exact: every e4m3 value is a bf16 value),
-// packed as two 16-byte groups of eight.
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4& raw, uint4& lo, uint4& hi) {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-            const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)(w[i] >> (16 * hlf));
-            const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3));
-            const float2 f = __half22float2(h);
-            const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-            o[2 * i + hlf] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-    }
-    lo = make_uint4(o[0], o[1], o[2], o[3]);
-    hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
 
 template <bool FP8, int STAGES, int NQT>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap q_map, int R, int R_step) {
+    verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap q_map, int R, int R_step, int raw_n) {
     constexpr int SC = s_cols<FP8>();
     constexpr int O_COL0 = o_col0<FP8>();
     using BR = Bars<STAGES>;
@@ -160,6 +147,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     extern __shared__ __align__(1024) uint8_t smem[];
     const Layout L = layout_for(R, nq_s, STAGES);
     const Misc M = misc_at(smem, L);
+    const int raw_off = align_up(L.total, 128);          // fp8 path: raw_n raw slots from here
     uint8_t* p_s = smem + L.p_off;
     const uint32_t q_addr = smem_u32(smem + L.q_off), kv_addr = smem_u32(smem + L.kv_off), p_addr = smem_u32(p_s);
 
@@ -197,33 +185,81 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int T = misaligned ? 0 : (k_end - k_begin + NK - 1) / NK;
     const int p = FP8 ? n : n - a.q_len;                 // first draft key (none on the fp8 path)
 
-    // ---- set-up: TMEM, barriers
+    // Streams usually fill their table row (n == slot_stride): the gather warps load the
+    // slot indices of their first two groups of tiles for the split range that length
+    // gives while seq_lens[b] is still in flight, and keep them when the real range is
+    // the same.  The indices read stay inside the stream's table row.
+    int spec_cur = 0, spec_nxt = 0;
+    bool spec_ok = false;
+    if (!FP8 && !a.balanced && warp >= 6) {
+        int gb, ge;
+        split_range(a.slot_stride, a.nsplit, s, NK, &gb, &ge);
+        const int Tg = (ge - gb + NK - 1) / NK;
+        const int32_t* srow = a.slot + (int64_t)b * a.slot_stride;
+        const int key = 8 * (warp - 6) + (lane & 7);
+        const int t0 = lane >> 3;
+        if (t0 < Tg) spec_cur = __ldg(srow + min(gb + t0 * NK + key, ge - 1));
+        if (t0 + 4 < Tg) spec_nxt = __ldg(srow + min(gb + (t0 + 4) * NK + key, ge - 1));
+        spec_ok = gb == k_begin && ge == k_end;
+    }
+
+    // ---- set-up.  Each role initialises the barriers it uses and starts its first cold
+    // loads before the block-wide barrier, so Q, the slot indices and the first key rows
+    // arrive in parallel instead of after it.  The gather warps only arrive at that barrier
+    // (they use no TMEM) and start copying as soon as their slot indices are in.
+    uint4 qraw[4 * 8];                                   // Q-to-TMEM warps: chunks 0 .. 3 of their row
     if (warp == 0) {
         tmem_alloc(M.tmem_slot, TMEM_COLS);
         tmem_relinquish();
-    }
-    if (tid == 32) {
-        for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&M.bars[B_KV_FULL + i], 32 * GATHER_WARPS);
-            mbar_init(&M.bars[B_KV_EMPTY + i], 1);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&M.bars[B_S_FULL + i], 1);
+                mbar_init(&M.bars[B_S_FREE + i], 128);
+            }
+            mbar_init(&M.bars[B_P_FULL], 128);
+            mbar_init(&M.bars[B_P_FULL + 1], 128);
+            mbar_init(&M.bars[B_Q_FULL], 1);
+            mbar_init(&M.bars[B_QT_FULL], 128);
+            mbar_init_fence();
+            // Q tile copies.  The bf16 path issues them before its key range is known (it
+            // depends on seq_lens); a CTA that turns out to have no keys waits for them
+            // before it exits.
+            if (!misaligned && (!FP8 || T > 0)) {
+                mbar_arrive_expect_tx(&M.bars[B_Q_FULL], (uint32_t)(nq_s * R * 128));
+                const int qrow = b * rows + row0;
+                for (int c = nq_t; c < NCHUNK; ++c)
+                    tma_load_2d(q_addr + (c - nq_t) * R * 128, &q_map, c * 64, qrow, &M.bars[B_Q_FULL]);
+            }
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&M.bars[B_S_FULL + i], 1);
-            mbar_init(&M.bars[B_S_FREE + i], 128);
+        __syncwarp();
+    } else if (warp >= 6) {
+        if (tid == 32 * 6) {
+            for (int i = 0; i < STAGES; ++i) {
+                mbar_init(&M.bars[B_KV_FULL + i], 32 * GATHER_WARPS);
+                mbar_init(&M.bars[B_KV_EMPTY + i], 1);
+            }
+            *M.abort = misaligned ? 1 : 0;
+            mbar_init_fence();
         }
-        mbar_init(&M.bars[B_P_FULL], 128);
-        mbar_init(&M.bars[B_P_FULL + 1], 128);
-        mbar_init(&M.bars[B_Q_FULL], 1);
-        mbar_init(&M.bars[B_QT_FULL], 128);
-        *M.abort = misaligned ? 1 : 0;
-        mbar_init_fence();
-        if (bad_len) atomicOr(a.status, DEV_BAD_LEN);
-        if (misaligned) atomicOr(a.status, DEV_TIMEOUT);
+        __syncwarp();
+        bar_sync(4, 32 * GATHER_WARPS);                  // the gather warps see their barriers
+        bar_arrive(3, NTHREADS);
+    } else if (!misaligned && nq_t > 0) {
+        // the TMEM chunks of Q row r (rows past the tile: zeros)
+        const int r = (warp & 3) * 32 + lane;
+        const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * rows + row0 + r) * D_QK);
+#pragma unroll
+        for (int j = 0; j < 8 * nq_t; ++j)
+            qraw[j] = r < nrows ? __ldg(qrow + j) : make_uint4(0u, 0u, 0u, 0u);
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *M.tmem_slot;
+    if (warp < 6) {
+        tc_fence_before();
+        __syncwarp();
+        bar_sync(3, NTHREADS);
+        tc_fence_after();
+    }
+    const uint32_t tmem = warp < 6 ? *M.tmem_slot : 0u;
 
     if (!FP8 && warp <= 1) {
         // ================= MMA issue, bf16: warp 0 Q K^T, warp 1 P V =================
@@ -233,14 +269,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // c3-64k -5%).  They write different TMEM columns (S buffers / O^T) and only read
         // shared memory; each commit tracks its own thread's MMAs.  The fp8 path keeps one
         // issuer (P V of tile i - 1 after Q K^T of tile i): split issue measured slower there.
-        if (warp == 1 && T > 0 && lane == 0) {
-            // the Q tile copies come first
-            mbar_arrive_expect_tx(&M.bars[B_Q_FULL], (uint32_t)(nq_s * R * 128));
-            const int qrow = b * rows + row0;
-            for (int c = nq_t; c < NCHUNK; ++c)
-                tma_load_2d(q_addr + (c - nq_t) * R * 128, &q_map, c * 64, qrow, &M.bars[B_Q_FULL]);
-        }
-        __syncwarp();
         if (T > 0) {
             const uint32_t id_qk = idesc_bf16(128, NK, false, false);
             const uint32_t id_pv = idesc_bf16(128, R, true, false);
@@ -313,6 +341,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             if (!ok && lane == 0) give_up(M, a.status);
+        } else if (warp == 1 && !misaligned) {
+            mbar_wait(&M.bars[B_Q_FULL], 0, M.abort);   // no keys: the Q copies must land before exit
         }
         __syncwarp();
     } else if (FP8 && warp == 0) {
@@ -390,13 +420,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         __syncwarp();
     } else if (FP8 && warp == 1) {
-        // ================= Q tile copies =================
-        if (T > 0 && lane == 0) {
-            mbar_arrive_expect_tx(&M.bars[B_Q_FULL], (uint32_t)(nq_s * R * 128));
-            const int qrow = b * rows + row0;
-            for (int c = nq_t; c < NCHUNK; ++c)
-                tma_load_2d(q_addr + (c - nq_t) * R * 128, &q_map, c * 64, qrow, &M.bars[B_Q_FULL]);
-        }
+        // Q tile copies were issued during set-up
     } else if (warp >= 6) {
         // ================= key-tile gather: keys 8w .. 8w+7 of every tile =================
         const int w = warp - 6;
@@ -412,25 +436,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int j = min(k_begin + t * NK + 8 * w + (lane & 7), k_end - 1);   // past the split: repeat a valid key
             return __ldg(slot_row + j);
         };
-        int cur = load_slots(0), nxt = load_slots(4);
-        // bf16 path: lane l copies 16-byte pieces f = l, l + 32, ... of the warp's 8 rows x
-        // 72 pieces; consecutive lanes take consecutive pieces of a row (contiguous reads)
-        for (int i = 0; i < T; ++i) {
-            const int st = i % STAGES;
-            if ((i & 3) == 0) {
-                if (i > 0) {
+        int cur = spec_cur, nxt = spec_nxt;
+        if (!spec_ok) {
+            cur = load_slots(0);
+            nxt = load_slots(4);
+        }
+        // Slot indices of the next tile to copy: groups advance with the copy position.
+        auto next_slots = [&](int j) -> int {
+            if ((j & 3) == 0) {
+                if (j > 0) {
                     cur = nxt;
-                    nxt = load_slots(i + 4);
+                    nxt = load_slots(j + 4);
                 }
                 if (cur < 0 || (int64_t)cur >= a.n_pool) { bad_slot = true; cur = 0; }
             }
-            const int sl = __shfl_sync(0xffffffffu, cur, ((i & 3) << 3) + (lane & 7));   // key 8 w + (lane & 7)
-            if (i >= STAGES && !mbar_wait(&M.bars[B_KV_EMPTY + st], ((i - STAGES) / STAGES) & 1, M.abort)) {
-                give_up(M, a.status);
-                break;
-            }
-            const uint32_t base = kv_addr + st * STAGE_BYTES;
-            if constexpr (!FP8) {
+            return __shfl_sync(0xffffffffu, cur, ((j & 3) << 3) + (lane & 7));   // key 8 w + (lane & 7)
+        };
+        if constexpr (!FP8) {
+            // lane l copies 16-byte pieces f = l, l + 32, ... of the warp's 8 rows x 72 pieces
+            // straight into the stage; consecutive lanes take consecutive pieces of a row
+            for (int i = 0; i < T; ++i) {
+                const int st = i % STAGES;
+                const int sl = next_slots(i);
+                if (i >= STAGES && !mbar_wait(&M.bars[B_KV_EMPTY + st], ((i - STAGES) / STAGES) & 1, M.abort)) {
+                    give_up(M, a.status);
+                    break;
+                }
+                const uint32_t base = kv_addr + st * STAGE_BYTES;
 #pragma unroll
                 for (int it = 0; it < 8 * (D_QK / 8) / 32; ++it) {      // 18 pieces per lane
                     const int f = it * 32 + lane;
@@ -441,42 +473,73 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     cp_async16(dst, a.kv + (int64_t)row_slot * D_QK + pc * 8);
                 }
                 if (!(a.debug_stall && i == 0)) cp_async_arrive_noinc(&M.bars[B_KV_FULL + st]);
-            } else {
-                // latent: row it of the warp's 8, lane = 16 e4m3 codes (dims 16 lane .. 16 lane + 15);
-                // rope: 8 rows x 8 pieces of 16 bytes, two per lane.  All loads first, then
-                // convert and store into the same swizzled layout as the bf16 path.
-                uint4 raw[8], rope[2];
+            }
+        } else {
+            // The raw rows (e4m3 latent, bf16 rope, fp32 scale) are copied raw_n - 1 tiles
+            // ahead into a ring of raw slots, so several tiles' reads are in flight; each
+            // warp then widens its own 8 keys into the swizzled bf16 stage.  Group k of
+            // every thread's cp.async groups holds tile k (or nothing past the last tile).
+            const uint32_t raw_addr = smem_u32(smem + raw_off);
+            auto copy_raw = [&](int j) {
+                const int sl = next_slots(j);
+                const uint32_t rb = raw_addr + (uint32_t)((j % raw_n) * RAW_SLOT);
 #pragma unroll
-                for (int it = 0; it < 8; ++it) {
+                for (int it = 0; it < 8; ++it) {         // latent: one 512-byte row per step
                     const int row_slot = __shfl_sync(0xffffffffu, sl, it);
-                    raw[it] = __ldg(reinterpret_cast<const uint4*>(a.kv_lat + (int64_t)row_slot * D_V) + lane);
+                    cp_async16(rb + (8 * w + it) * D_V + lane * 16, a.kv_lat + (int64_t)row_slot * D_V + lane * 16);
                 }
 #pragma unroll
-                for (int it = 0; it < 2; ++it) {
+                for (int it = 0; it < 2; ++it) {         // rope: 8 rows x 8 pieces of 16 bytes
                     const int f = it * 32 + lane;
                     const int row_slot = __shfl_sync(0xffffffffu, sl, f >> 3);
-                    rope[it] = __ldg(reinterpret_cast<const uint4*>(a.kv_rope + (int64_t)row_slot * 64) + (f & 7));
+                    cp_async16(rb + RAW_ROPE + (8 * w + (f >> 3)) * 128 + (f & 7) * 16,
+                               a.kv_rope + (int64_t)row_slot * 64 + (f & 7) * 8);
                 }
-                const float ksc = lane < 8 ? __ldg(a.kv_scale + sl) : 0.f;
-                if (lane < 8) M.kscale[st * NK + 8 * w + lane] = ksc;
+                if (lane < 8) cp_async4(rb + RAW_SCALE + (8 * w + lane) * 4, a.kv_scale + sl);
+            };
+            for (int j = 0; j < raw_n - 1; ++j) {
+                if (j < T) copy_raw(j);
+                cp_async_commit();
+            }
+            // lane l widens dims 16 l .. 16 l + 15: 16-byte pieces j0, j0 + 1 of region l / 4.
+            // Lanes of odd regions store their second piece first, so each store covers all
+            // eight 16-byte bank groups (four lanes each) instead of four.
+            const int region = lane >> 2, j0 = (lane & 3) * 2, odd = region & 1;
+            for (int i = 0; i < T; ++i) {
+                const int st = i % STAGES;
+                if (i + raw_n - 1 < T) copy_raw(i + raw_n - 1);   // into the slot tile i - 1 used
+                cp_async_commit();
+                cp_async_wait_pending(raw_n - 1);                 // tile i has landed (this thread)
+                __syncwarp();                                     // ... for the whole warp
+                if (i >= STAGES && !mbar_wait(&M.bars[B_KV_EMPTY + st], ((i - STAGES) / STAGES) & 1, M.abort)) {
+                    give_up(M, a.status);
+                    break;
+                }
+                const uint8_t* rb = smem + raw_off + (i % raw_n) * RAW_SLOT;
                 uint8_t* sbase = smem + L.kv_off + st * STAGE_BYTES;
 #pragma unroll
                 for (int it = 0; it < 8; ++it) {
                     const int key = 8 * w + it;
-                    uint4 lo, hi;
-                    e4m3x16_to_bf16(raw[it], lo, hi);
-                    const int region = lane >> 2, j0 = (lane & 3) * 2;
-                    *reinterpret_cast<uint4*>(sbase + region * REGION + key * 128 + ((j0 ^ (key & 7)) << 4)) = lo;
-                    *reinterpret_cast<uint4*>(sbase + region * REGION + key * 128 + (((j0 + 1) ^ (key & 7)) << 4)) = hi;
+                    const uint4 raw = *reinterpret_cast<const uint4*>(rb + key * D_V + lane * 16);
+                    const uint4 r = odd ? make_uint4(raw.z, raw.w, raw.x, raw.y) : raw;
+                    uint4 first, second;
+                    e4m3x16_to_bf16(r, first, second);
+                    uint8_t* row = sbase + region * REGION + key * 128;
+                    *reinterpret_cast<uint4*>(row + (((j0 + odd) ^ (key & 7)) << 4)) = first;
+                    *reinterpret_cast<uint4*>(row + (((j0 + 1 - odd) ^ (key & 7)) << 4)) = second;
                 }
 #pragma unroll
                 for (int it = 0; it < 2; ++it) {
                     const int f = it * 32 + lane;
                     const int key = 8 * w + (f >> 3), c = f & 7;
-                    *reinterpret_cast<uint4*>(sbase + 8 * REGION + key * 128 + ((c ^ (key & 7)) << 4)) = rope[it];
+                    *reinterpret_cast<uint4*>(sbase + 8 * REGION + key * 128 + ((c ^ (key & 7)) << 4)) =
+                        *reinterpret_cast<const uint4*>(rb + RAW_ROPE + key * 128 + c * 16);
                 }
-                fence_proxy_async_smem();              // generic stores -> tensor-core reads
+                if (lane < 8)
+                    M.kscale[st * NK + 8 * w + lane] = *reinterpret_cast<const float*>(rb + RAW_SCALE + (8 * w + lane) * 4);
+                fence_proxy_async_smem();                         // generic stores -> tensor-core reads
                 if (!(a.debug_stall && i == 0)) mbar_arrive(&M.bars[B_KV_FULL + st]);
+                __syncwarp();                                     // raw slot read before it is refilled
             }
         }
         cp_async_wait_all();
@@ -500,29 +563,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-        if (T > 0) {
-            // Q chunks 0 .. nq_t-1 of row r into TMEM lane r (rows past the tile: zeros),
-            // two chunks (sixteen 16-byte loads) in flight at a time
-            const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * rows + row0 + r) * D_QK);
-            for (int c0 = 0; c0 < nq_t; c0 += 2) {
-                uint4 raw[16];
+        if (!misaligned) {
+            // Q chunks 0 .. nq_t-1 of row r (loaded during set-up) into TMEM lane r
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const bool have = row_ok && c0 + (j >> 3) < nq_t;
-                    raw[j] = have ? __ldg(qrow + c0 * 8 + j) : make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < nq_t; ++c) {
+                uint32_t v[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    v[4 * j] = qraw[8 * c + j].x; v[4 * j + 1] = qraw[8 * c + j].y;
+                    v[4 * j + 2] = qraw[8 * c + j].z; v[4 * j + 3] = qraw[8 * c + j].w;
                 }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (c0 + h < nq_t) {
-                        uint32_t v[32];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            v[4 * j] = raw[8 * h + j].x; v[4 * j + 1] = raw[8 * h + j].y;
-                            v[4 * j + 2] = raw[8 * h + j].z; v[4 * j + 3] = raw[8 * h + j].w;
-                        }
-                        tmem_st32(tmem + lane_base + Q_COL0 + (c0 + h) * 32, v);
-                    }
-                }
+                tmem_st32(tmem + lane_base + Q_COL0 + c * 32, v);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -678,6 +729,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_before();
     __syncthreads();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (tid == 32) {
+        if (bad_len) atomicOr(a.status, DEV_BAD_LEN);
+        if (misaligned) atomicOr(a.status, DEV_TIMEOUT);
+    }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -696,8 +751,9 @@ namespace {
 constexpr int MAX_SMEM = 232448;                     // opt-in shared memory per block on sm_103
 
 // Instantiations: (fp8, key stages, Q chunks in TMEM).  q_tmem_chunks gives 4 for up to
-// 80 rows on the bf16 path and for up to 64 on the fp8 path, 2 beyond that (0 for fp8
-// at 96 rows); four stages fit whenever four or more chunks leave shared memory.
+// 80 rows on the bf16 path and for up to 64 on the fp8 path, 2 beyond that; four bf16
+// stages fit whenever four or more chunks leave shared memory.  The fp8 path keeps fewer
+// bf16 stages (3 at <= 64 rows, 2 at 80) so that three or four raw slots fit beside them.
 template <bool FP8, int STAGES, int NQT>
 cudaError_t launch_one(bool set_attr, dim3 grid, cudaStream_t stream, const VerifyArgs& a, const CUtensorMap& q_map,
                        int R, int R_step) {
@@ -706,9 +762,17 @@ cudaError_t launch_one(bool set_attr, dim3 grid, cudaStream_t stream, const Veri
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SMEM);
         if (e != cudaSuccess) return e;
     }
-    const int smem = layout_for(R, NCHUNK - NQT, STAGES).total;
+    int smem = layout_for(R, NCHUNK - NQT, STAGES).total;
+    int raw_n = 0;
+    if (FP8) {                                       // as many raw slots as still fit
+        smem = align_up(smem, 128);
+        raw_n = (MAX_SMEM - smem) / RAW_SLOT;
+        raw_n = raw_n > MAX_RAW_SLOTS ? MAX_RAW_SLOTS : raw_n;
+        if (raw_n < 1) return cudaErrorInvalidConfiguration;
+        smem += raw_n * RAW_SLOT;
+    }
     if (smem > MAX_SMEM) return cudaErrorInvalidConfiguration;
-    k<<<grid, NTHREADS, smem, stream>>>(a, q_map, R, R_step);
+    k<<<grid, NTHREADS, smem, stream>>>(a, q_map, R, R_step, raw_n);
     return cudaGetLastError();
 }
 }  // namespace
@@ -722,8 +786,8 @@ cudaError_t launch_verify_tc(const VerifyArgs& a_in, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     int n_tiles, R_step, R;
-    // fp8: at 96 rows no TMEM is left for Q and the shared-memory Q tile, three key
-    // stages and two P buffers exceed the opt-in limit, so its tiles stop at 80 rows
+    // fp8: at 96 rows no TMEM is left for Q and the shared-memory Q tile, the key stages
+    // and two P buffers exceed the opt-in limit, so its tiles stop at 80 rows
     tc_tiling(a.q_len * a.H, a.kv_fp8 ? 80 : MAX_R, &n_tiles, &R_step, &R);
     const int nq = q_tmem_chunks(a.kv_fp8, R) >= 4 ? 4 : q_tmem_chunks(a.kv_fp8, R) >= 2 ? 2 : 0;
     const bool four = layout_for(R, NCHUNK - nq, 4).total <= MAX_SMEM;
@@ -742,12 +806,9 @@ cudaError_t launch_verify_tc(const VerifyArgs& a_in, cudaStream_t stream) {
                          : cudaErrorInvalidConfiguration; break;
         case 1: e = four ? cudaErrorInvalidConfiguration
                          : launch_one<false, 3, 2>(set, grid, stream, a, q_map, R, R_step); break;
-        case 2: e = four ? launch_one<true, 4, 4>(set, grid, stream, a, q_map, R, R_step)
-                         : cudaErrorInvalidConfiguration; break;
-        case 3: e = four ? launch_one<true, 4, 2>(set, grid, stream, a, q_map, R, R_step)
-                         : cudaErrorInvalidConfiguration; break;
-        default: e = four ? cudaErrorInvalidConfiguration
-                          : launch_one<true, 3, 0>(set, grid, stream, a, q_map, R, R_step); break;
+        case 2: e = launch_one<true, 3, 4>(set, grid, stream, a, q_map, R, R_step); break;
+        case 3: e = launch_one<true, 2, 2>(set, grid, stream, a, q_map, R, R_step); break;
+        default: e = cudaErrorInvalidConfiguration; break;   // unreachable: fp8 tiles stop at 80 rows
     }
     if (e == cudaSuccess) attr_set[dev][which] = true;
     return e;

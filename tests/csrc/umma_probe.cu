@@ -12,8 +12,12 @@
 // tma_tile_probe: rows [row0, row0 + R) of a [n, 576] bf16 matrix loaded with nine
 //   2-D tile copies (box 64 columns x R rows, 128-byte swizzle) into nine regions of
 //   R x 128 B; the raw shared-memory bytes are copied out.
+// fp8_decode_probe: the fp8 key path's e4m3 -> bf16 decoder applied to n codes (n a
+//   multiple of 16), sixteen per thread, bf16 bit patterns out.
 #include <cuda_bf16.h>
 #include <stdint.h>
+
+#include "../../mla_speculative_verify_attention_gb300/csrc/fp8_decode.cuh"
 
 #include "../../mla_speculative_verify_attention_gb300/csrc/tc_ptx.cuh"
 #include "../../mla_speculative_verify_attention_gb300/csrc/tmap.h"
@@ -168,7 +172,25 @@ __global__ void __launch_bounds__(128) tma_probe_kernel(const __grid_constant__ 
         reinterpret_cast<uint4*>(out)[i] = ok ? reinterpret_cast<const uint4*>(smem)[i] : make_uint4(0, 0, 0, 0);
 }
 
+__global__ void fp8_decode_kernel(const uint4* codes, uint4* out, int groups) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= groups) return;
+    uint4 lo, hi;
+    mla::e4m3x16_to_bf16(codes[i], lo, hi);
+    out[2 * i] = lo;
+    out[2 * i + 1] = hi;
+}
+
 }  // namespace
+
+// codes: n e4m3 bytes, out: n bf16 bit patterns; both device pointers, 16-byte aligned
+extern "C" int fp8_decode_probe(const uint8_t* codes, uint16_t* out, int n, cudaStream_t stream) {
+    if (n <= 0 || n % 16 || ((uintptr_t)codes | (uintptr_t)out) % 16) return -2;
+    const int groups = n / 16;
+    fp8_decode_kernel<<<(groups + 127) / 128, 128, 0, stream>>>(reinterpret_cast<const uint4*>(codes),
+                                                               reinterpret_cast<uint4*>(out), groups);
+    return cudaGetLastError() == cudaSuccess ? 0 : -6;
+}
 
 extern "C" int umma_probe(const uint16_t* A, const uint16_t* B, float* D, int N, int K, int a_mode, int a_sw,
                           int b_sw, int swap, int* status, cudaStream_t stream) {

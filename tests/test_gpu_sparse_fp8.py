@@ -33,7 +33,10 @@ def test_c5_full(cuda_lib):
 
 
 @pytest.mark.parametrize("nsplit", [1, 3, 0])
-@pytest.mark.parametrize("shape", [(3, 16, 77), (2, 64, 300), (1, 1, 40), (2, 128, 65), (4, 8, 1), (2, 96, 100)],
+# 80 rows: two bf16 stages beside three raw slots; 32 rows, 700 keys: four raw slots, the
+# ring wrapping many times, and a ragged last tile
+@pytest.mark.parametrize("shape", [(3, 16, 77), (2, 64, 300), (1, 1, 40), (2, 128, 65), (4, 8, 1), (2, 96, 100),
+                                   (2, 80, 290), (1, 32, 700)],
                          ids=lambda s: f"B{s[0]}H{s[1]}k{s[2]}")
 def test_shapes(cuda_lib, shape, nsplit):
     B, H, topk = shape

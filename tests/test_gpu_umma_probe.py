@@ -5,7 +5,10 @@
   with A held in TMEM,
   read back from TMEM, against a float64 matmul of the same bf16 values;
 * a TMA 2-D tile load (box 64 x R, 128-byte swizzle): the exact shared-memory bytes
-  against the swizzled arrangement computed here."""
+  against the swizzled arrangement computed here;
+* the fp8 key path's e4m3 -> bf16 decoder: every one of the 256 codes, in every byte
+  position of a 16-code group, against the OCP E4M3 value the oracle decodes (NaN codes
+  must give NaN)."""
 import ctypes
 import os
 import subprocess
@@ -32,6 +35,8 @@ def probe():
     L.umma_probe.restype = I
     L.tma_tile_probe.argtypes = [P, ctypes.c_longlong, I, I, P, P, P]
     L.tma_tile_probe.restype = I
+    L.fp8_decode_probe.argtypes = [P, P, I, P]
+    L.fp8_decode_probe.restype = I
     return L
 
 
@@ -111,3 +116,26 @@ def test_tma_tile_rows_into_sw128(probe, R):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert np.array_equal(out.cpu().numpy(), _expected_sw128(src[row0:row0 + R], R))
+
+
+def test_fp8_decode_every_code_every_position(probe):
+    import oracle
+    rng = np.random.default_rng(5)
+    # 16 rotations put each code in each byte position; then random groups, half of
+    # them NaN-free, so both the bit path and the NaN path run beside one another
+    base = np.arange(256, dtype=np.uint8)
+    groups = [np.roll(base, k) for k in range(16)]
+    rnd = rng.integers(0, 256, size=(4096, 16), dtype=np.uint8)
+    rnd[::2] &= np.where((rnd[::2] & 0x7F) == 0x7F, 0xFE, 0xFF).astype(np.uint8)
+    codes = np.concatenate([np.concatenate(groups), rnd.reshape(-1)])
+    dev = torch.device("cuda", 0)
+    c = torch.from_numpy(codes).to(dev)
+    out = torch.empty(codes.size, dtype=torch.int16, device=dev)
+    assert probe.fp8_decode_probe(c.data_ptr(), out.data_ptr(), codes.size, None) == 0
+    torch.cuda.synchronize()
+    got = out.cpu().view(torch.bfloat16).float().numpy().astype(np.float64)
+    want = oracle.e4m3_to_f64(codes)
+    nan = np.isnan(want)
+    assert nan.sum() > 0 and np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))    # -0 stays -0

@@ -68,7 +68,12 @@ constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns: S buffers first (bf16 path: two of 32 columns; fp8 path: two pairs
 // of latent / rope scores), then O^T
 template <bool FP8> constexpr int s_cols() { return FP8 ? 2 * NK : NK; }
-template <bool FP8> constexpr int o_col0() { return 2 * s_cols<FP8>(); }
+// S buffers: the bf16 path double-buffers S so Q K^T of the next tile can run ahead of
+// the softmax; the fp8 path's single issuer reaches Q K^T of tile i + 1 only after P V of
+// tile i - 1, by which time the softmax has long read S of tile i, so one buffer costs it
+// nothing and leaves two more Q chunks' worth of TMEM columns.
+template <bool FP8> constexpr int s_bufs() { return FP8 ? 1 : 2; }
+template <bool FP8> constexpr int o_col0() { return s_bufs<FP8>() * s_cols<FP8>(); }
 constexpr float TAU = 8.0f;                          // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -79,7 +84,7 @@ template <int STAGES> struct Bars {
                          P_FULL = 2 * STAGES + 4, Q_FULL = 2 * STAGES + 6, QT_FULL = 2 * STAGES + 7,
                          COUNT = 2 * STAGES + 8;    // P_FULL: one per P buffer
 };
-static_assert(Bars<2>::COUNT * 8 <= 128 && Bars<3>::COUNT * 8 <= 128 && Bars<4>::COUNT * 8 <= 128, "barrier area");
+static_assert(Bars<3>::COUNT * 8 <= 128 && Bars<4>::COUNT * 8 <= 128, "barrier area");
 
 struct Layout {
     int q_off, kv_off, p_off, misc_off, total;
@@ -103,7 +108,7 @@ __host__ __device__ inline Layout layout_for(int R, int nq_s, int stages) {
 
 // TMEM columns left for Q chunks (32 columns each) beside the S buffers and O^T.
 __host__ __device__ inline int q_tmem_chunks(bool fp8, int R) {
-    const int used = 2 * (fp8 ? 2 * NK : NK) + 4 * R;
+    const int used = (fp8 ? s_bufs<true>() * s_cols<true>() : s_bufs<false>() * s_cols<false>()) + 4 * R;
     const int c = ((int)TMEM_COLS - used) / 32;
     return c < 0 ? 0 : (c > NCHUNK ? NCHUNK : c);
 }
@@ -137,12 +142,14 @@ template <bool FP8, int STAGES, int NQT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap q_map, int R, int R_step, int raw_n) {
     constexpr int SC = s_cols<FP8>();
+    constexpr int SB = s_bufs<FP8>();
     constexpr int O_COL0 = o_col0<FP8>();
     using BR = Bars<STAGES>;
     constexpr int B_KV_FULL = BR::KV_FULL, B_KV_EMPTY = BR::KV_EMPTY, B_S_FULL = BR::S_FULL,
                   B_S_FREE = BR::S_FREE, B_P_FULL = BR::P_FULL, B_Q_FULL = BR::Q_FULL, B_QT_FULL = BR::QT_FULL;
     constexpr int nq_t = NQT;                            // Q chunks 0 .. NQT-1 live in TMEM,
     constexpr int nq_s = NCHUNK - NQT;                   // chunks NQT .. 8 in shared memory
+    constexpr int NQ0 = nq_t < 4 ? nq_t : 4;             // TMEM chunks loaded before the set-up barrier
     const int Q_COL0 = O_COL0 + 4 * R;                   // Q chunk c < nq_t: TMEM columns Q_COL0 + 32 c ..
     extern __shared__ __align__(1024) uint8_t smem[];
     const Layout L = layout_for(R, nq_s, STAGES);
@@ -207,7 +214,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // loads before the block-wide barrier, so Q, the slot indices and the first key rows
     // arrive in parallel instead of after it.  The gather warps only arrive at that barrier
     // (they use no TMEM) and start copying as soon as their slot indices are in.
-    uint4 qraw[4 * 8];                                   // Q-to-TMEM warps: chunks 0 .. 3 of their row
+    uint4 qraw[4 * 8];                                   // Q-to-TMEM warps: chunks 0 .. NQ0-1 of their row
     if (warp == 0) {
         tmem_alloc(M.tmem_slot, TMEM_COLS);
         tmem_relinquish();
@@ -246,11 +253,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bar_sync(4, 32 * GATHER_WARPS);                  // the gather warps see their barriers
         bar_arrive(3, NTHREADS);
     } else if (!misaligned && nq_t > 0) {
-        // the TMEM chunks of Q row r (rows past the tile: zeros)
+        // the first TMEM chunks of Q row r (rows past the tile: zeros)
         const int r = (warp & 3) * 32 + lane;
         const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * rows + row0 + r) * D_QK);
 #pragma unroll
-        for (int j = 0; j < 8 * nq_t; ++j)
+        for (int j = 0; j < 8 * NQ0; ++j)
             qraw[j] = r < nrows ? __ldg(qrow + j) : make_uint4(0u, 0u, 0u, 0u);
     }
     if (warp < 6) {
@@ -311,13 +318,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int i = 0; i < T && ok; ++i) {
                     const int st = i % STAGES;
                     ok = mbar_wait(&M.bars[B_KV_FULL + st], (i / STAGES) & 1, M.abort);
-                    if (ok && i >= 2) ok = mbar_wait(&M.bars[B_S_FREE + (i & 1)], ((i - 2) >> 1) & 1, M.abort);
+                    if (ok && i >= SB) ok = mbar_wait(&M.bars[B_S_FREE + i % SB], ((i - SB) / SB) & 1, M.abort);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     fence_proxy_async_smem();          // cp.async (generic proxy) data -> tensor-core reads
                     tc_fence_after();
                     const uint64_t st16 = (uint64_t)(st * STAGE_BYTES) >> 4;
-                    const uint32_t d_s = tmem + (i & 1) * SC;
+                    const uint32_t d_s = tmem + (i % SB) * SC;
                     if (elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < D_QK / 16; ++ks) {
@@ -335,7 +342,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             mma_bf16(d, dq + qo, dk + st16 + ko, id_qk, acc);
                         }
                     }
-                    mma_commit(&M.bars[B_S_FULL + (i & 1)]);
+                    mma_commit(&M.bars[B_S_FULL + i % SB]);
                     }
                     __syncwarp();
                 }
@@ -386,13 +393,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int i = 0; i < T && ok; ++i) {
                 const int st = i % STAGES;
                 ok = mbar_wait(&M.bars[B_KV_FULL + st], (i / STAGES) & 1, M.abort);
-                if (ok && i >= 2) ok = mbar_wait(&M.bars[B_S_FREE + (i & 1)], ((i - 2) >> 1) & 1, M.abort);
+                if (ok && i >= SB) ok = mbar_wait(&M.bars[B_S_FREE + i % SB], ((i - SB) / SB) & 1, M.abort);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 fence_proxy_async_smem();              // cp.async (generic proxy) data -> tensor-core reads
                 tc_fence_after();
                 const uint64_t st16 = (uint64_t)(st * STAGE_BYTES) >> 4;
-                const uint32_t d_s = tmem + (i & 1) * SC;
+                const uint32_t d_s = tmem + (i % SB) * SC;
                 if (elect_one()) {
 #pragma unroll
                 for (int ks = 0; ks < D_QK / 16; ++ks) {
@@ -410,7 +417,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         mma_bf16(d, dq + qo, dk + st16 + ko, id_qk, acc);
                     }
                 }
-                mma_commit(&M.bars[B_S_FULL + (i & 1)]);
+                mma_commit(&M.bars[B_S_FULL + i % SB]);
                 }
                 __syncwarp();
                 if (i >= 1) issue_pv(i - 1);
@@ -515,13 +522,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     give_up(M, a.status);
                     break;
                 }
+                // All reads of the raw slot first: the compiler cannot tell the raw slot from
+                // the stage it writes, so reads placed after a store would wait for it.
                 const uint8_t* rb = smem + raw_off + (i % raw_n) * RAW_SLOT;
+                uint4 raw[8], rope[2];
+#pragma unroll
+                for (int it = 0; it < 8; ++it)
+                    raw[it] = *reinterpret_cast<const uint4*>(rb + (8 * w + it) * D_V + lane * 16);
+#pragma unroll
+                for (int it = 0; it < 2; ++it) {
+                    const int f = it * 32 + lane;
+                    rope[it] = *reinterpret_cast<const uint4*>(rb + RAW_ROPE + (8 * w + (f >> 3)) * 128 + (f & 7) * 16);
+                }
+                const float ksc = lane < 8 ? *reinterpret_cast<const float*>(rb + RAW_SCALE + (8 * w + lane) * 4) : 0.f;
                 uint8_t* sbase = smem + L.kv_off + st * STAGE_BYTES;
 #pragma unroll
                 for (int it = 0; it < 8; ++it) {
                     const int key = 8 * w + it;
-                    const uint4 raw = *reinterpret_cast<const uint4*>(rb + key * D_V + lane * 16);
-                    const uint4 r = odd ? make_uint4(raw.z, raw.w, raw.x, raw.y) : raw;
+                    const uint4 r = odd ? make_uint4(raw[it].z, raw[it].w, raw[it].x, raw[it].y) : raw[it];
                     uint4 first, second;
                     e4m3x16_to_bf16(r, first, second);
                     uint8_t* row = sbase + region * REGION + key * 128;
@@ -532,11 +550,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int it = 0; it < 2; ++it) {
                     const int f = it * 32 + lane;
                     const int key = 8 * w + (f >> 3), c = f & 7;
-                    *reinterpret_cast<uint4*>(sbase + 8 * REGION + key * 128 + ((c ^ (key & 7)) << 4)) =
-                        *reinterpret_cast<const uint4*>(rb + RAW_ROPE + key * 128 + c * 16);
+                    *reinterpret_cast<uint4*>(sbase + 8 * REGION + key * 128 + ((c ^ (key & 7)) << 4)) = rope[it];
                 }
-                if (lane < 8)
-                    M.kscale[st * NK + 8 * w + lane] = *reinterpret_cast<const float*>(rb + RAW_SCALE + (8 * w + lane) * 4);
+                if (lane < 8) M.kscale[st * NK + 8 * w + lane] = ksc;
                 fence_proxy_async_smem();                         // generic stores -> tensor-core reads
                 if (!(a.debug_stall && i == 0)) mbar_arrive(&M.bars[B_KV_FULL + st]);
                 __syncwarp();                                     // raw slot read before it is refilled
@@ -564,16 +580,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
         if (!misaligned) {
-            // Q chunks 0 .. nq_t-1 of row r (loaded during set-up) into TMEM lane r
-#pragma unroll
-            for (int c = 0; c < nq_t; ++c) {
+            // Q chunks 0 .. nq_t-1 of row r into TMEM lane r: chunks 0 .. NQ0-1 were loaded
+            // during set-up, the rest follow two at a time
+            auto store_chunk = [&](int c, int slot) {
                 uint32_t v[32];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    v[4 * j] = qraw[8 * c + j].x; v[4 * j + 1] = qraw[8 * c + j].y;
-                    v[4 * j + 2] = qraw[8 * c + j].z; v[4 * j + 3] = qraw[8 * c + j].w;
+                    v[4 * j] = qraw[8 * slot + j].x; v[4 * j + 1] = qraw[8 * slot + j].y;
+                    v[4 * j + 2] = qraw[8 * slot + j].z; v[4 * j + 3] = qraw[8 * slot + j].w;
                 }
                 tmem_st32(tmem + lane_base + Q_COL0 + c * 32, v);
+            };
+#pragma unroll
+            for (int c = 0; c < NQ0; ++c) store_chunk(c, c);
+            const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * rows + row0 + r) * D_QK);
+#pragma unroll
+            for (int c0 = NQ0; c0 < nq_t; c0 += 2) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (c0 + (j >> 3) < nq_t) qraw[j] = row_ok ? __ldg(qrow + c0 * 8 + j) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    if (c0 + h < nq_t) store_chunk(c0 + h, h);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -584,16 +612,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int i = 0; i < T; ++i) {
-            ok = mbar_wait(&M.bars[B_S_FULL + (i & 1)], (i >> 1) & 1, M.abort);
+            ok = mbar_wait(&M.bars[B_S_FULL + i % SB], (i / SB) & 1, M.abort);
             if (bar_red_or(1, 128, !ok)) { ok = false; break; }
             tc_fence_after();
             uint32_t sv[NK];
-            tmem_ld32(tmem + lane_base + (i & 1) * SC, sv);
+            tmem_ld32(tmem + lane_base + (i % SB) * SC, sv);
             float ksc[FP8 ? NK : 1];
             if constexpr (FP8) {
                 // s = scale * (scale_t * q_lat . k8 + q_rope . k_rope)
                 uint32_t sr[NK];
-                tmem_ld32(tmem + lane_base + (i & 1) * SC + NK, sr);
+                tmem_ld32(tmem + lane_base + (i % SB) * SC + NK, sr);
                 tmem_ld_wait();
                 // the key scales were written before the tile's kv_full arrival
                 ok = mbar_wait(&M.bars[B_KV_FULL + i % STAGES], (i / STAGES) & 1, M.abort);
@@ -606,7 +634,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tmem_ld_wait();
             }
             tc_fence_before();
-            mbar_arrive(&M.bars[B_S_FREE + (i & 1)]);
+            mbar_arrive(&M.bars[B_S_FREE + i % SB]);
 
             const int k0 = k_begin + i * NK;
             float x[NK];
@@ -751,9 +779,9 @@ namespace {
 constexpr int MAX_SMEM = 232448;                     // opt-in shared memory per block on sm_103
 
 // Instantiations: (fp8, key stages, Q chunks in TMEM).  q_tmem_chunks gives 4 for up to
-// 80 rows on the bf16 path and for up to 64 on the fp8 path, 2 beyond that; four bf16
-// stages fit whenever four or more chunks leave shared memory.  The fp8 path keeps fewer
-// bf16 stages (3 at <= 64 rows, 2 at 80) so that three or four raw slots fit beside them.
+// 80 rows on the bf16 path, 2 beyond that; the fp8 path (one S buffer) takes 6 up to 64
+// rows and 4 at 80.  Four bf16 stages fit whenever four or more chunks leave shared
+// memory; the fp8 path keeps three so that two to four raw slots fit beside them.
 template <bool FP8, int STAGES, int NQT>
 cudaError_t launch_one(bool set_attr, dim3 grid, cudaStream_t stream, const VerifyArgs& a, const CUtensorMap& q_map,
                        int R, int R_step) {
@@ -789,7 +817,8 @@ cudaError_t launch_verify_tc(const VerifyArgs& a_in, cudaStream_t stream) {
     // fp8: at 96 rows no TMEM is left for Q and the shared-memory Q tile, the key stages
     // and two P buffers exceed the opt-in limit, so its tiles stop at 80 rows
     tc_tiling(a.q_len * a.H, a.kv_fp8 ? 80 : MAX_R, &n_tiles, &R_step, &R);
-    const int nq = q_tmem_chunks(a.kv_fp8, R) >= 4 ? 4 : q_tmem_chunks(a.kv_fp8, R) >= 2 ? 2 : 0;
+    const int qt = q_tmem_chunks(a.kv_fp8, R);
+    const int nq = a.kv_fp8 ? (qt >= 6 ? 6 : qt >= 4 ? 4 : 0) : (qt >= 4 ? 4 : qt >= 2 ? 2 : 0);
     const bool four = layout_for(R, NCHUNK - nq, 4).total <= MAX_SMEM;
     CUtensorMap q_map;
     const uint64_t q_rows = (uint64_t)a.B * a.q_len * a.H;
@@ -799,15 +828,15 @@ cudaError_t launch_verify_tc(const VerifyArgs& a_in, cudaStream_t stream) {
     dim3 grid(a.nsplit, n_tiles, a.balanced ? 1 : a.B);
     int which;
     if (!a.kv_fp8) which = nq == 4 ? 0 : 1;
-    else which = nq == 4 ? 2 : nq == 2 ? 3 : 4;
+    else which = nq == 6 ? 2 : nq == 4 ? 3 : 4;
     const bool set = !attr_set[dev][which];
     switch (which) {
         case 0: e = four ? launch_one<false, 4, 4>(set, grid, stream, a, q_map, R, R_step)
                          : cudaErrorInvalidConfiguration; break;
         case 1: e = four ? cudaErrorInvalidConfiguration
                          : launch_one<false, 3, 2>(set, grid, stream, a, q_map, R, R_step); break;
-        case 2: e = launch_one<true, 3, 4>(set, grid, stream, a, q_map, R, R_step); break;
-        case 3: e = launch_one<true, 2, 2>(set, grid, stream, a, q_map, R, R_step); break;
+        case 2: e = launch_one<true, 3, 6>(set, grid, stream, a, q_map, R, R_step); break;
+        case 3: e = launch_one<true, 3, 4>(set, grid, stream, a, q_map, R, R_step); break;
         default: e = cudaErrorInvalidConfiguration; break;   // unreachable: fp8 tiles stop at 80 rows
     }
     if (e == cudaSuccess) attr_set[dev][which] = true;

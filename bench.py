@@ -427,7 +427,11 @@ def run_gpu(args):
 
     def timed_loop(n, fn, flush_l2=True):
         """n calls of fn(), each bracketed by CUDA events on the launching stream; L2 flushed
-        before each call (outside the events) unless flush_l2 is False.  Returns ms per call."""
+        before each call (outside the events) unless flush_l2 is False.  Returns ms per call.
+        With the flush each step ends with a synchronize: the flush then keeps the GPU busy
+        while the host submits the call, so the events never time the GPU waiting for the
+        host (a loop that queued every step at once measured c4 at 222 us per call against
+        72 us once the host fell behind).  Without it the steps queue back to back."""
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
         torch.cuda.synchronize(dev)
         for i in range(n):
@@ -436,6 +440,8 @@ def run_gpu(args):
             ev[i][0].record(stream)
             fn()
             ev[i][1].record(stream)
+            if flush_l2:
+                torch.cuda.synchronize(dev)
         torch.cuda.synchronize(dev)
         return [a.elapsed_time(b) for a, b in ev]
 

@@ -7,7 +7,10 @@
 //            stage; arrivals are asynchronous, so a warp moves on to the next tile
 //            while its copies are in flight (measured on GB300: random 1152-byte
 //            rows gather about twice as fast this way as with TMA tile::gather4,
-//            whose per-instruction cost caps a 512-byte gather)
+//            whose per-instruction cost caps a 512-byte gather).  fp8 keys: the raw
+//            rows (e4m3 latent, bf16 rope, fp32 scale) go by cp.async into a ring of
+//            raw slots a few tiles ahead, and each warp widens its keys into the
+//            same bf16 stage layout
 //   S        = Q K^T: tcgen05.mma M=128 (query rows) x N=32 (keys) x K=576, fp32 in TMEM;
 //            the first 64-dim chunks of Q sit in TMEM (A operand read from tensor
 //            memory, no shared-memory traffic), the rest in shared memory
@@ -18,10 +21,11 @@
 //            softmax of tile i overlaps P V of tile i - 1
 //   O^T     += V^T P^T: tcgen05.mma M=128 (value dims) x N=rows x K=32 (keys), four
 //            128-dim chunks, fp32 accumulators resident in TMEM
-// Computing P V transposed keeps O^T in 4 x rows <= 384 TMEM columns, so two S
-// buffers (64 columns) fit beside it in the 512-column TMEM and Q K^T runs once
-// per tile; the columns left over hold as many 32-column Q chunks as fit (4 for up
-// to 80 rows).  Measured on GB300, an M=128 x N=32 x K=16 MMA issued from a
+// Computing P V transposed keeps O^T in 4 x rows <= 384 TMEM columns, so the S
+// buffers fit beside it in the 512-column TMEM and Q K^T runs once per tile (bf16:
+// two S buffers of 32 columns; fp8: one of 64, latent and rope scores apart); the
+// columns left over hold as many 32-column Q chunks as fit (bf16: 4 for up to 80
+// rows; fp8: 6 for up to 64).  Measured on GB300, an M=128 x N=32 x K=16 MMA issued from a
 // converged warp takes ~17 cycles with A in TMEM and ~40 with A in shared memory
 // (bound by shared-memory reads of the 4 KB A tile), so every Q chunk moved to TMEM
 // takes four MMAs off the shared-memory port, and the freed shared memory buys a
@@ -37,6 +41,9 @@
 //               TMEM lane) and the epilogue (thread = value dim = TMEM lane of O^T);
 //               TMEM lane quadrant = warp % 4
 //   warps 6-9   key-tile gather into a 3- or 4-stage ring; warp 6 + w copies keys 8w .. 8w+7
+// Every role initialises its own mbarriers and starts its first cold reads (Q, slot
+// indices, key rows) before the block-wide set-up barrier, which the gather warps only
+// arrive at.
 // The pages' sm_120 designs (head-tile amortisation, warp-per-key dot products,
 // NSPLIT tuning) are replaced by packing heads x drafts as MMA rows, a slot-table
 // gather sized to the SM's load path, and the split-count policy of the host code.

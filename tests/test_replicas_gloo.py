@@ -48,3 +48,14 @@ def test_single_process_is_identity():
     import bench
     assert bench.max_over_ranks([3.0, 4.0]) == [3.0, 4.0]
     assert bench.aggregate_throughput(2e9, 1.0, 1) == pytest.approx(2000.0)
+
+
+def test_kernel_hash_ignores_comments_but_not_code():
+    """The committed DRAM counters stay valid across comment edits, never across code edits."""
+    import bench
+    code = "int f(int x) {\n    return x + 1;   // add one\n}\n"
+    commented = "// header\n/* block\n   comment */\nint f(int x) {\n\n    return x + 1;\n}\n"
+    assert bench._code_only(code) == bench._code_only(commented)
+    assert bench._code_only(code) != bench._code_only(code.replace("x + 1", "x + 2"))
+    h = bench.kernel_source_hash()
+    assert len(h) == 16 and h == bench.kernel_source_hash()

@@ -67,6 +67,16 @@ def test_edge_shapes(cuda_lib, cfg, nsplit):
     check(cuda_lib, inp, nsplit=nsplit)
 
 
+@pytest.mark.parametrize("nsplit", [0, 1, 3, 16])
+def test_padded_slot_table(cuda_lib, nsplit):
+    """One stream whose slot-table row is much wider than its length: the set-up guesses
+    the split range from the row width, loads those indices early, and must discard them
+    (and read no key past the stream's length)."""
+    inp = w.make_verify("padded", 1, 9, 8, [3000], seed=71, n_pool=8192, scattered=True,
+                        mask_kind="tree", slot_stride=5000)
+    check(cuda_lib, inp, nsplit=nsplit)
+
+
 def test_mask_is_applied(cuda_lib):
     """Draft rows x50 make the mask decisive (oracle outputs for two masks differ by O(1)):
     the GPU must follow the mask it is given, for both masks."""

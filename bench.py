@@ -13,8 +13,9 @@ every step, outside the events.  The split kernel alone is timed the same way in
 a second loop (its duration is the roofline's denominator), and a warm-L2 loop
 (no flush) is reported beside it.  `e2e` is the same metric end to end: the
 step's inputs (queries, slot table, lengths, mask and the new draft KV rows)
-copied from pinned host memory, the KV append kernel, the verify call and the
-outputs copied back, all inside the timed region.  `--impl reference` times the
+copied from one pinned host buffer in one copy, the KV append kernel, the verify
+call and the outputs (out and lse, one buffer) copied back, all inside the timed
+region.  `--impl reference` times the
 fp64 CPU oracle on this host's cores instead (the reference arm).
 """
 from __future__ import annotations
@@ -275,6 +276,25 @@ def run_reference(args):
 # workloads as seen by the GPU arm: device inputs, the split stage, the full call,
 # and the per-step host -> device inputs of the end-to-end measurement
 # --------------------------------------------------------------------------
+def stage_inputs(named, dev):
+    """[(name, pinned host tensor)] -> (pinned host buffer, device buffer, {name: device
+    view}): every input in its own 256-byte-aligned section of one buffer, so a step's
+    inputs cross in one copy (as a serving runtime stages them) instead of one copy each."""
+    import torch
+    offs, total = [], 0
+    for _, h in named:
+        offs.append(total)
+        total += (h.numel() * h.element_size() + 255) // 256 * 256
+    hbuf = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = {}
+    for (name, h), off in zip(named, offs):
+        n = h.numel() * h.element_size()
+        hbuf[off:off + n].copy_(h.contiguous().view(-1).view(torch.uint8))
+        views[name] = dbuf[off:off + n].view(h.dtype).view(h.shape)
+    return hbuf, dbuf, views
+
+
 class VerifyWorkload:
     def __init__(self, inp, mv, dev):
         import torch
@@ -296,24 +316,29 @@ class VerifyWorkload:
         self.mv.verify_attn(self.q, self.kv, self.st, self.sl, self.mk, self.inp.scale, out=out, lse=lse,
                             nsplit=ns, workspace=ws, stream=stream)
 
-    def host_inputs(self):
-        """(pinned host tensor, device tensor to fill) pairs: queries, slot table, lengths,
-        mask and the q_len new draft KV rows of every stream ([B, q_len, 576], staged for
-        the KV append kernel, which writes them into their pool slots)."""
+    def stage(self):
+        """A step's inputs in one pinned buffer and one device buffer: queries, slot table,
+        lengths, mask and the q_len new draft KV rows of every stream ([B, q_len, 576],
+        staged for the KV append kernel, which writes them into their pool slots).  The
+        call's tensors are rebound to views of the device buffer.  Returns (host, device)."""
         import torch
         inp = self.inp
-        pairs = [(torch.from_numpy(inp.q_bits.view(np.int16)).pin_memory(), self.q.view(torch.int16)),
-                 (torch.from_numpy(np.ascontiguousarray(inp.slot_table)).pin_memory(), self.st),
-                 (torch.from_numpy(np.ascontiguousarray(inp.seq_lens)).pin_memory(), self.sl)]
+        named = [("q", torch.from_numpy(inp.q_bits.view(np.int16))),
+                 ("st", torch.from_numpy(np.ascontiguousarray(inp.slot_table))),
+                 ("sl", torch.from_numpy(np.ascontiguousarray(inp.seq_lens)))]
         if self.mk is not None:
-            pairs.append((torch.from_numpy(np.ascontiguousarray(inp.mask)).pin_memory(), self.mk))
+            named.append(("mk", torch.from_numpy(np.ascontiguousarray(inp.mask))))
         rows = np.empty((inp.B, inp.q_len, 576), np.uint16)
         for b in range(inp.B):
             n = int(inp.seq_lens[b])
             rows[b] = inp.kv_bits[inp.slot_table[b, n - inp.q_len:n]]
-        self.new_rows = torch.empty(rows.shape, dtype=torch.bfloat16, device=self.dev)
-        pairs.append((torch.from_numpy(rows.view(np.int16)).pin_memory(), self.new_rows.view(torch.int16)))
-        return pairs
+        named.append(("new_rows", torch.from_numpy(rows.view(np.int16))))
+        hbuf, dbuf, v = stage_inputs(named, self.dev)
+        self.q, self.st, self.sl = v["q"].view(torch.bfloat16), v["st"], v["sl"]
+        if self.mk is not None:
+            self.mk = v["mk"]
+        self.new_rows = v["new_rows"].view(torch.bfloat16)
+        return hbuf, dbuf
 
     def before_call(self, stream):
         """KV append of the staged draft rows (end-to-end step only); returns launches."""
@@ -347,23 +372,24 @@ class Fp8Workload:
         self.mv.sparse_fp8_decode(self.q, self.lat, self.sc, self.rope, self.ts, self.f.scale, out=out.view(self.B, self.H, 512),
                                   lse=lse.view(self.B, self.H), nsplit=ns, workspace=ws, stream=stream)
 
-    def host_inputs(self):
-        """Queries, top-k lists and the one new token row per stream (latent codes, scale,
-        rope; staged contiguously and written into the pool by the fp8 append kernel)."""
+    def stage(self):
+        """A step's inputs in one pinned buffer and one device buffer: queries, top-k lists
+        and the one new token row per stream (latent codes, scale, rope; written into the
+        pool by the fp8 append kernel).  Returns (host, device)."""
         import torch
         f = self.f
-        pairs = [(torch.from_numpy(f.q_bits.view(np.int16)).pin_memory(), self.q.view(torch.int16)),
-                 (torch.from_numpy(np.ascontiguousarray(f.topk_slots)).pin_memory(), self.ts)]
         rows = np.ascontiguousarray(f.topk_slots[:, 0])
-        self.new_slots = torch.empty(rows.shape, dtype=torch.int32, device=self.dev)
-        self.new_lat = torch.empty((f.B, 512), dtype=torch.uint8, device=self.dev)
-        self.new_sc = torch.empty((f.B,), dtype=torch.float32, device=self.dev)
-        self.new_rope = torch.empty((f.B, 64), dtype=torch.bfloat16, device=self.dev)
-        pairs += [(torch.from_numpy(rows).pin_memory(), self.new_slots),
-                  (torch.from_numpy(f.kv_lat[rows].copy()).pin_memory(), self.new_lat),
-                  (torch.from_numpy(f.kv_scale[rows].copy()).pin_memory(), self.new_sc),
-                  (torch.from_numpy(f.kv_rope[rows].view(np.int16).copy()).pin_memory(), self.new_rope.view(torch.int16))]
-        return pairs
+        named = [("q", torch.from_numpy(f.q_bits.view(np.int16))),
+                 ("ts", torch.from_numpy(np.ascontiguousarray(f.topk_slots))),
+                 ("new_slots", torch.from_numpy(rows)),
+                 ("new_lat", torch.from_numpy(f.kv_lat[rows].copy())),
+                 ("new_sc", torch.from_numpy(f.kv_scale[rows].copy())),
+                 ("new_rope", torch.from_numpy(f.kv_rope[rows].view(np.int16).copy()))]
+        hbuf, dbuf, v = stage_inputs(named, self.dev)
+        self.q, self.ts = v["q"].view(torch.bfloat16), v["ts"]
+        self.new_slots, self.new_lat, self.new_sc = v["new_slots"], v["new_lat"], v["new_sc"]
+        self.new_rope = v["new_rope"].view(torch.bfloat16)
+        return hbuf, dbuf
 
     def before_call(self, stream):
         """fp8 KV append of the staged new rows (end-to-end step only); returns launches."""
@@ -481,21 +507,21 @@ def run_gpu(args):
     status = mv.device_status(stream)
 
     # end to end through the C ABI with host buffers: this step's inputs copied from
-    # pinned memory, the KV append (verify path), the call (mla_verify_attn /
-    # mla_sparse_fp8_decode), and D2H of out and lse, all inside the events
-    pairs = wl.host_inputs()
-    h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
-    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+    # pinned memory (one staged buffer), the KV append (verify path), the call
+    # (mla_verify_attn / mla_sparse_fp8_decode), and D2H of out and lse (one buffer), all
+    # inside the events
+    h_in, d_in = wl.stage()
+    d_res = torch.empty(out.numel() + lse.numel(), dtype=torch.float32, device=dev)
+    out_e, lse_e = d_res[:out.numel()].view(out.shape), d_res[out.numel():].view(lse.shape)
+    h_res = torch.empty(d_res.numel(), dtype=torch.float32).pin_memory()
+    h2d = h_in.numel()
+    d2h = h_res.numel() * 4
 
     def e2e_step():
-        for h, d in pairs:
-            d.copy_(h, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         wl.before_call(stream)
-        wl.full(call_ns, ws, out, lse, stream)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        wl.full(call_ns, ws, out_e, lse_e, stream)
+        h_res.copy_(d_res, non_blocking=True)
 
     for _ in range(3):
         e2e_step()

@@ -17,6 +17,9 @@ __global__ void __launch_bounds__(APPEND_THREADS)
     kv_append_kernel(__nv_bfloat16* __restrict__ kv, const int32_t* __restrict__ slot, int slot_stride,
                      const int32_t* __restrict__ seq_lens, const __nv_bfloat16* __restrict__ new_kv, int B,
                      int q_len, int64_t n_pool, unsigned* status) {
+    // the verify kernel that usually follows may become resident now; its
+    // griddepcontrol.wait still holds it until this grid's writes are visible
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long warp = ((long long)blockIdx.x * APPEND_THREADS + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= (long long)B * q_len) return;
@@ -43,6 +46,7 @@ __global__ void __launch_bounds__(APPEND_THREADS)
                          __nv_bfloat16* __restrict__ kv_rope, int64_t n_pool, const int32_t* __restrict__ slots,
                          const uint8_t* __restrict__ new_lat, const float* __restrict__ new_scale,
                          const __nv_bfloat16* __restrict__ new_rope, int n_rows, unsigned* status) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // as in kv_append_kernel
     const long long i = ((long long)blockIdx.x * APPEND_THREADS + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (i >= n_rows) return;

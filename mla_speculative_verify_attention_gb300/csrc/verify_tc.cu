@@ -159,6 +159,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr int NQ0 = nq_t < 4 ? nq_t : 4;             // TMEM chunks loaded before the set-up barrier
     const int Q_COL0 = O_COL0 + 4 * R;                   // Q chunk c < nq_t: TMEM columns Q_COL0 + 32 c ..
     extern __shared__ __align__(1024) uint8_t smem[];
+    // Launched as a programmatic dependent of the previous kernel on the stream (the KV
+    // append, typically): the CTAs become resident while it drains, and wait here until
+    // it has completed and its writes are visible, before the first global read.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const Layout L = layout_for(R, nq_s, STAGES);
     const Misc M = misc_at(smem, L);
     const int raw_off = align_up(L.total, 128);          // fp8 path: raw_n raw slots from here
@@ -807,7 +811,18 @@ cudaError_t launch_one(bool set_attr, dim3 grid, cudaStream_t stream, const Veri
         smem += raw_n * RAW_SLOT;
     }
     if (smem > MAX_SMEM) return cudaErrorInvalidConfiguration;
-    k<<<grid, NTHREADS, smem, stream>>>(a, q_map, R, R_step, raw_n);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see griddepcontrol.wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, a, q_map, R, R_step, raw_n);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 }  // namespace

@@ -28,7 +28,11 @@
  *  - Tensor pointers are DEVICE pointers owned by the caller; the library keeps
  *    none of them after the call returns and allocates no device memory.
  *  - Work is enqueued on `stream` (NULL = the legacy default stream).  No entry
- *    point synchronises except mla_verify_status(), which says so.
+ *    point synchronises except mla_verify_status(), which says so.  The attention
+ *    kernels are launched as programmatic dependents of the kernel before them on the
+ *    stream and wait for its completion (and the visibility of its writes) before
+ *    reading any input, so stream order is kept; the KV-append kernels let the
+ *    attention kernel that follows them become resident early.
  *  - Return value: MLA_OK (0) or a negative mla_status.  Argument errors are
  *    detected on the host before anything is enqueued.  Errors that only the
  *    device can see (a slot index outside [0, n_pool), a seq_len outside

@@ -171,15 +171,21 @@ class Clocks:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, csv_path: str | None = None):
+        """Samples nvidia-smi every 100 ms into csv_path (a temporary file when None)."""
         self.index = index
         self.proc = None
-        self.path = None
+        self.path = csv_path
+        self.temporary = csv_path is None
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{self.index}.csv")
+            if self.path is None:
+                import tempfile
+                fd, self.path = tempfile.mkstemp(prefix=f"clocks_gpu{self.index}_", suffix=".csv")
+                os.close(fd)
+            else:
+                os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
@@ -208,6 +214,8 @@ class Clocks:
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+        if self.temporary:
+            os.remove(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
@@ -492,7 +500,7 @@ def run_gpu(args):
         split_kernel()
     torch.cuda.synchronize(dev)
 
-    clocks = Clocks(local)
+    clocks = Clocks(local, None if args.clocks_csv is None else args.clocks_csv.replace("{gpu}", str(local)))
     clocks.start()
     time.sleep(0.25)
     K = args.steps
@@ -607,6 +615,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the nvidia-smi clock samples of the timed region in this file ({gpu} = GPU index)")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)

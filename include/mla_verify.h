@@ -249,15 +249,20 @@ int mla_sparse_fp8_partials(const void* q, const uint8_t* kv_lat_e4m3, const flo
  * pages have no counterpart of this entry point.
  *
  * Same arguments and result as mla_verify_attn() minus the workspace.  The
- * KV-split partials go to a file-scope device array of MLA_STATIC_SCRATCH_BYTES
- * that every GPU loading this library holds until the process exits; nothing
- * is allocated per call (no cudaMalloc, no cudaFree, no allocating library
+ * KV-split partials go to a file-scope device array of MLA_STATIC_SCRATCH_BYTES.
+ * A device holds that array from the moment the library's device code is loaded
+ * there until the process exits: under CUDA's default lazy module loading at the
+ * latest from the first static-scratch call on that device, and on every device
+ * from its context's creation when CUDA_MODULE_LOADING=EAGER.  Nothing is
+ * allocated per call (no cudaMalloc, no cudaFree, no allocating library
  * routine).  With nsplit = 0 the split count is chosen to fit the array; an
  * explicit nsplit whose partials need more than MLA_STATIC_SCRATCH_BYTES
  * (mla_verify_workspace_bytes) returns MLA_ERR_WORKSPACE.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  All calls on a device share the one array and it keeps
+ * any stream capture.  The address is cached per device ordinal for the device's
+ * primary context (the CUDA runtime's context): the entry point supports that
+ * context only, and must not be used again after cudaDeviceReset.  All calls on a device share the one array and it keeps
  * the last call's contents (every call overwrites what it reads, so nothing
  * needs clearing); calls whose GPU work overlaps -- on different streams, or
  * from different host threads -- race on it and must be serialised by the caller.
@@ -288,6 +293,19 @@ int mla_verify_version(void);
  * hang, and the context stays usable.  One-shot; returns MLA_OK.
  */
 int mla_debug_stall_next_launch(void);
+
+/*
+ * Test counter of the online softmax's lazy rescale.  The kernels keep a running
+ * row maximum and rescale the resident output accumulator only when a later key
+ * tile raises some row's maximum by more than 2^8 (about 5.5 in natural-log units);
+ * every (CTA, key tile) on which that happens adds one to a per-device counter.
+ * This reads it (with clear != 0 also resets it to zero) so that a test can show
+ * that its inputs really drove the rescale path.  SYNCHRONISES `stream`.  Returns
+ * MLA_OK, MLA_ERR_NULL (count is NULL) or MLA_ERR_DEVICE.  No counterpart in the
+ * pages: the online softmax with a running maximum is theirs, the counter is a
+ * test aid.
+ */
+int mla_debug_rescale_count(mla_stream_t stream, uint64_t* count, int clear);
 
 #ifdef __cplusplus
 }

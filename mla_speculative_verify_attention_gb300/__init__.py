@@ -34,7 +34,7 @@ EXPORTS = ("mla_verify_workspace_bytes", "mla_verify_auto_nsplit", "mla_verify_a
            "mla_verify_partials", "mla_verify_combine", "mla_verify_status",
            "mla_status_string", "mla_verify_version", "mla_verify_attn_static_scratch",
            "mla_sparse_fp8_decode", "mla_sparse_fp8_partials", "mla_verify_attn_packed", "mla_kv_append", "mla_kv_append_fp8",
-           "mla_debug_stall_next_launch")
+           "mla_debug_stall_next_launch", "mla_debug_rescale_count")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
@@ -89,6 +89,8 @@ def load():
     L.mla_verify_version.restype = I
     L.mla_debug_stall_next_launch.argtypes = []
     L.mla_debug_stall_next_launch.restype = I
+    L.mla_debug_rescale_count.argtypes = [P, ctypes.POINTER(ctypes.c_uint64), I]
+    L.mla_debug_rescale_count.restype = I
     _lib = L
     return L
 
@@ -332,4 +334,13 @@ def device_status(stream=None, clear: bool = True) -> int:
     """Reads (and clears) the device status word; synchronises the stream."""
     v = ctypes.c_uint32(0)
     _check("mla_verify_status", load().mla_verify_status(_stream(stream), ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)
+
+
+def debug_rescale_count(stream=None, clear: bool = True) -> int:
+    """Reads (and clears) the per-device count of (CTA, key tile) pairs on which the
+    online softmax rescaled its output accumulator; synchronises the stream."""
+    v = ctypes.c_uint64(0)
+    _check("mla_debug_rescale_count",
+           load().mla_debug_rescale_count(_stream(stream), ctypes.byref(v), 1 if clear else 0))
     return int(v.value)

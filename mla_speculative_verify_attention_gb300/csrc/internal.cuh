@@ -34,6 +34,7 @@ struct VerifyArgs {
     float* part_lse;              // [B, q_len, H, nsplit]
     int nsplit;                   // uniform splits per stream, or (balanced) split slots
     unsigned* status;             // device status word
+    unsigned long long* rescales; // test counter: tiles on which a CTA rescaled its O^T accumulator
     // balanced split (several streams of unequal length, see balanced_plan): grid.x =
     // nsplit slots shared by all streams; partials are slot-major,
     // part_out [nsplit][q_len * H][512], part_lse [nsplit][q_len * H]

@@ -14,6 +14,9 @@ namespace mla {
 
 // Per-device status word of MLA_DEV_* bits (sticky until mla_verify_status clears it).
 __device__ unsigned g_status;
+// Per-device count of O^T rescales of the online softmax (read by tests through
+// mla_debug_rescale_count; the kernels only ever add to it).
+__device__ unsigned long long g_rescales;
 
 // Test hook: the next split-kernel launch withholds its first key-tile arrival.
 static std::atomic<bool> g_debug_stall{false};
@@ -23,6 +26,7 @@ namespace {
 
 constexpr int MAX_DEVICES = 64;
 unsigned* g_status_ptr[MAX_DEVICES];
+unsigned long long* g_rescales_ptr[MAX_DEVICES];
 int g_num_sms[MAX_DEVICES];
 int g_arch_ok[MAX_DEVICES];      // 0 unknown, 1 sm_103, -1 other
 
@@ -39,6 +43,8 @@ int device_state(int* dev_out, unsigned** status, int* num_sms) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return MLA_ERR_DEVICE;
         g_status_ptr[dev] = static_cast<unsigned*>(p);
+        if (cudaGetSymbolAddress(&p, g_rescales) != cudaSuccess) return MLA_ERR_DEVICE;
+        g_rescales_ptr[dev] = static_cast<unsigned long long*>(p);
         g_num_sms[dev] = sms;
         g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
     }
@@ -252,8 +258,8 @@ int run_verify(bool combine, const void* q, const void* kv, int64_t n_pool, cons
     if (rc != MLA_OK) return rc;
     if (B == 0) return MLA_OK;
     unsigned* status = nullptr;
-    int num_sms = 0;
-    rc = device_state(nullptr, &status, &num_sms);
+    int num_sms = 0, dev = 0;
+    rc = device_state(&dev, &status, &num_sms);
     if (rc != MLA_OK) return rc;
     int ns = nsplit > 0 ? nsplit : mla_verify_auto_nsplit(B, q_len, H, slot_stride, num_sms, ws ? ws_bytes : 0);
     const long long rows = (long long)B * q_len * H;
@@ -272,6 +278,7 @@ int run_verify(bool combine, const void* q, const void* kv, int64_t n_pool, cons
     a.out = out; a.lse = lse;
     a.nsplit = ns;
     a.status = status;
+    a.rescales = g_rescales_ptr[dev];
     // Several streams of unequal length with the automatic split count: cut all their
     // keys into equal chunks over one wave of CTAs (balanced split) when the workspace
     // holds its slot-major partials; the uniform per-stream split otherwise.
@@ -318,8 +325,8 @@ int run_sparse_fp8(bool combine, const void* q, const uint8_t* kv_lat, const flo
         !aligned(topk_slots, 4) || !aligned(out, 16) || !aligned(lse, 4))
         return MLA_ERR_ALIGN;
     unsigned* status = nullptr;
-    int num_sms = 0;
-    int rc = device_state(nullptr, &status, &num_sms);
+    int num_sms = 0, dev = 0;
+    int rc = device_state(&dev, &status, &num_sms);
     if (rc != MLA_OK) return rc;
     // automatic split count: every stream has the same topk keys, so one wave of CTAs
     // (no second wave to even out unequal lengths), at least 128 keys per split
@@ -349,6 +356,7 @@ int run_sparse_fp8(bool combine, const void* q, const uint8_t* kv_lat, const flo
     a.out = out; a.lse = lse;
     a.nsplit = ns;
     a.status = status;
+    a.rescales = g_rescales_ptr[dev];
     a.kv_fp8 = 1;
     a.kv_lat = kv_lat;
     a.kv_scale = kv_scale;
@@ -502,6 +510,24 @@ int mla_verify_status(mla_stream_t stream, uint32_t* device_status, int clear) {
         if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_DEVICE;
     }
     *device_status = v;
+    return MLA_OK;
+}
+
+int mla_debug_rescale_count(mla_stream_t stream, uint64_t* count, int clear) {
+    if (!count) return MLA_ERR_NULL;
+    int dev = 0;
+    int rc = device_state(&dev, nullptr, nullptr);
+    if (rc != MLA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned long long v = 0;
+    if (cudaMemcpyAsync(&v, g_rescales_ptr[dev], sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MLA_ERR_DEVICE;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_DEVICE;
+    if (clear) {
+        if (cudaMemsetAsync(g_rescales_ptr[dev], 0, sizeof v, s) != cudaSuccess) return MLA_ERR_DEVICE;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_DEVICE;
+    }
+    *count = (uint64_t)v;
     return MLA_OK;
 }
 

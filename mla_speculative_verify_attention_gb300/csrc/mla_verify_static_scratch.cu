@@ -5,11 +5,16 @@
 // arena that must not be bypassed), and latency-critical loops where an
 // allocation, which can implicitly synchronise the device or fail under memory
 // pressure, is not permitted.  This entry point needs no workspace from them:
-// the KV-split partials live in a file-scope device array that the library
-// reserves when it is loaded.
+// the KV-split partials live in a file-scope device array that is part of the
+// library's device code.
 //
-// The array holds MLA_STATIC_SCRATCH_BYTES (64 MiB).  Every GPU that loads the
-// library keeps that much device memory until the process exits.
+// The array holds MLA_STATIC_SCRATCH_BYTES (64 MiB).  A device holds it from the
+// moment this translation unit's device code is loaded there until the process
+// exits: with CUDA's default lazy module loading that is at the latest the first
+// static-scratch call on that device, with CUDA_MODULE_LOADING=EAGER it is the
+// creation of the device's context.
+#include <atomic>
+
 #include "../../include/mla_verify.h"
 #include "internal.cuh"
 
@@ -22,7 +27,12 @@ static_assert(kScratchBytes % 256 == 0, "scratch size must keep 256-byte section
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices];     // device address of g_scratch, per device (set up once)
+// Device address of g_scratch per device ordinal, looked up once per device.  Host
+// threads may make their first call on a device at the same time: they look up and
+// store the same value, so relaxed atomics suffice.  The address belongs to the
+// device's primary context (the one the CUDA runtime uses); it is not valid in
+// another context on that device nor after cudaDeviceReset.
+std::atomic<void*> g_scratch_ptr[kMaxDevices];
 
 }  // namespace
 
@@ -39,15 +49,15 @@ extern "C" int mla_verify_attn_static_scratch(const void* q, const void* kv_cach
                                        q_len, H, scale, out, lse, nsplit, nullptr, 0, stream);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_DEVICE;
-    if (g_scratch_ptr[dev] == nullptr) {
+    void* scratch = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (scratch == nullptr) {
         // One-time set-up on this device (the device is current): in host code the
         // array's name is only a host-side stand-in, so take its device address.
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return MLA_ERR_DEVICE;
-        g_scratch_ptr[dev] = p;
+        if (cudaGetSymbolAddress(&scratch, g_scratch) != cudaSuccess || scratch == nullptr) return MLA_ERR_DEVICE;
+        g_scratch_ptr[dev].store(scratch, std::memory_order_relaxed);
     }
     // The split stage writes every partial (empty splits included) before the
     // combine reads it, so nothing in the array needs clearing between calls.
     return mla_verify_attn(q, kv_cache, n_pool, slot_table, slot_stride, seq_lens, draft_mask, B, q_len, H, scale,
-                           out, lse, nsplit, g_scratch_ptr[dev], kScratchBytes, stream);
+                           out, lse, nsplit, scratch, kScratchBytes, stream);
 }

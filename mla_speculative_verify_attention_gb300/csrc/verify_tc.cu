@@ -682,6 +682,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (bar_red_or(1, 128, !ok)) { ok = false; break; }
             if (any && i >= 1) {
                 // O^T column r (query row r) *= alpha_r; thread = TMEM lane = value dim
+                if (r == 0) atomicAdd(a.rescales, 1ull);
                 M.alpha[r] = alpha;
                 bar_sync(2, 128);
                 tc_fence_after();

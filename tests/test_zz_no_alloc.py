@@ -3,16 +3,17 @@ device memory (plugins inside a runtime that owns all device memory, latency-cri
 loops that must not call cudaMalloc/cudaFree).  Its KV-split partials live in the
 library's file-scope device array instead of a caller workspace.
 
-Checked through the C ABI against mla_verify_attn (the entry point with a caller
-workspace), within the parity tolerances of the other GPU tests, on two calls in a
-row -- the second with other inputs, so stale contents of the shared array cannot
-leak into a result.  This file is collected last."""
+Checked through the C ABI against the fp64 oracle and against mla_verify_attn (the
+entry point with a caller workspace), within the parity tolerances of the other GPU
+tests, on two calls in a row -- the second with other inputs, so stale contents of
+the shared array cannot leak into a result.  This file is collected last."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as w
 from gpu_util import compare, to_device
 
@@ -43,6 +44,8 @@ def test_static_scratch_matches_workspace_entry_point_twice(cuda_lib, nsplit):
     second = w.make_verify("na2", 1, 9, 64, [2000], seed=82, mask_kind="chain")
     for inp in (first, second):
         out, lse, ro, rl = _call(mv, inp, nsplit)
+        exact_o, exact_l = oracle.verify_inputs(inp)
+        compare(out, lse, exact_o, exact_l, what=f"{inp.name} nsplit={nsplit} vs oracle")
         compare(out, lse, ro.double().cpu().numpy(), rl.double().cpu().numpy(), what=f"{inp.name} nsplit={nsplit}")
     assert mv.device_status() == 0
 

@@ -8,8 +8,10 @@ Prints ONE JSON line.  A step is one verify call through the C ABI
 workload (default c2: 1 stream, q_len 9, H 64, prefix 4096, contiguous slots,
 causal chain -- the pages' microbenchmark shape).  `value` is effective KV
 bandwidth (KV-row bytes / time) with inputs resident in HBM, timed with CUDA
-events per step on the launching stream; L2 is flushed (256 MiB written) before
-every step, outside the events.  The split kernel alone is timed the same way in
+events per step on the launching stream; L2 is flushed before every step, outside
+the events: 256 MiB are written and then another 256 MiB buffer is read, so none of
+the call's inputs is in L2 and the flush leaves no dirty line whose write-back would
+fall inside the timed call (a write-only flush is timed too and reported beside it).  The split kernel alone is timed the same way in
 a second loop (its duration is the roofline's denominator), and a warm-L2 loop
 (no flush) is reported beside it.  `e2e` is the same metric end to end: the
 step's inputs (queries, slot table, lengths, mask and the new draft KV rows)
@@ -465,12 +467,24 @@ def run_gpu(args):
     out = torch.empty((B, q_len, H, 512), dtype=torch.float32, device=dev)
     lse = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sum = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2_lines(i, clean=True):
+        """Evict L2: write 256 MiB (> 2x L2); then, unless clean is False, read another
+        256 MiB, which writes the dirty flush lines back and leaves L2 holding clean lines
+        of a buffer the call never touches."""
+        flush.fill_(float(i))
+        if clean:
+            torch.sum(flush_rd, dim=0, out=flush_sum)
     stream = torch.cuda.current_stream(dev)
     launches_per_step = 1 + (1 if ns > 1 else 0)
 
-    def timed_loop(n, fn, flush_l2=True):
+    def timed_loop(n, fn, flush_l2=True, clean=True):
         """n calls of fn(), each bracketed by CUDA events on the launching stream; L2 flushed
-        before each call (outside the events) unless flush_l2 is False.  Returns ms per call.
+        before each call (outside the events) unless flush_l2 is False (clean=False: the
+        write-only flush, whose dirty lines are written back during the call).  Returns ms
+        per call.
         With the flush each step ends with a synchronize: the flush then keeps the GPU busy
         while the host submits the call, so the events never time the GPU waiting for the
         host (a loop that queued every step at once measured c4 at 222 us per call against
@@ -479,7 +493,7 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
         for i in range(n):
             if flush_l2:
-                flush.fill_(float(i))
+                flush_l2_lines(i, clean)
             ev[i][0].record(stream)
             fn()
             ev[i][1].record(stream)
@@ -495,7 +509,7 @@ def run_gpu(args):
         wl.partials(call_ns, ws, out, lse, stream)
 
     for _ in range(max(args.warmup, 3)):
-        flush.fill_(1.0)
+        flush_l2_lines(1)
         full_call()
         split_kernel()
     torch.cuda.synchronize(dev)
@@ -512,6 +526,7 @@ def run_gpu(args):
     wall_dev = time.perf_counter() - wall0
     kern_ms = timed_loop(min(K, 500), split_kernel)        # the split (attention) kernel alone
     warm_ms = timed_loop(min(K, 200), full_call, flush_l2=False)
+    dirty_ms = timed_loop(min(K, 200), full_call, clean=False)
     status = mv.device_status(stream)
 
     # end to end through the C ABI with host buffers: this step's inputs copied from
@@ -541,8 +556,9 @@ def run_gpu(args):
     mean_kern = statistics.mean(kern_ms)
     mean_e2e = statistics.mean(e2e_ms)
     mean_warm = statistics.mean(warm_ms)
-    mean_step, mean_kern, mean_e2e, mean_warm = max_over_ranks([mean_step, mean_kern, mean_e2e, mean_warm],
-                                                               device=dev)
+    mean_dirty = statistics.mean(dirty_ms)
+    mean_step, mean_kern, mean_e2e, mean_warm, mean_dirty = max_over_ranks(
+        [mean_step, mean_kern, mean_e2e, mean_warm, mean_dirty], device=dev)
     value = aggregate_throughput(work["kv_bytes"], mean_step, world)
     e2e_value = aggregate_throughput(work["kv_bytes"], mean_e2e, world)
 
@@ -577,11 +593,13 @@ def run_gpu(args):
         "dtype": "bf16", "data": "synthetic (seeded SplitMix64 / Box-Muller inputs, shapes of the pages' workloads)",
         "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "B": B, "q_len": q_len,
                    "H": H, "keys": work["keys"], "nsplit": ns, "split": split_desc,
-                   "l2": "flushed before every step (256 MiB write, outside the timed events)",
+                   "l2": "flushed before every step, outside the timed events: 256 MiB written, then "
+                         "another 256 MiB read (no dirty flush line left to write back inside the call)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "us_per_call": mean_step * 1e3,
         "us_per_call_p10_p50_p90": [srt[int(0.1 * (K - 1))] * 1e3, srt[(K - 1) // 2] * 1e3, srt[int(0.9 * (K - 1))] * 1e3],
         "us_per_call_warm_l2": mean_warm * 1e3,
+        "us_per_call_write_only_flush": mean_dirty * 1e3,
         "roofline_us": rl_us, "roofline_pct": 100.0 * rl_us / (mean_step * 1e3),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": traffic_from_profiles(args.config), "kernel": "split (attention) kernel",
@@ -609,7 +627,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="c2", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--config", default="c4", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--nsplit", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -136,10 +136,16 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __rest
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
     const float L = mx + logf(zs);
+    float wl = 0.f;
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) {
         for (int s0 = 0; s0 < S; s0 += CB_BATCH * Z) {
+            // weights of this warp's next 32 splits, one per lane, handed out by shuffles
+            if ((s0 / (CB_BATCH * Z)) % (32 / CB_BATCH) == 0) {
+                const int s = s0 + z + Z * lane;
+                wl = s < S ? expf(__ldg(pl + s * lse_step) - L) : 0.f;
+            }
             if (s0 > 0) {
 #pragma unroll
                 for (int m = 0; m < CB_BATCH; ++m) {
@@ -147,11 +153,12 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float* __rest
                     if (s < S) v[m] = __ldg(reinterpret_cast<const float4*>(base + (long long)s * out_step));
                 }
             }
+            const int lane0 = ((s0 / (CB_BATCH * Z)) % (32 / CB_BATCH)) * CB_BATCH;
 #pragma unroll
             for (int m = 0; m < CB_BATCH; ++m) {
                 const int s = s0 + z + Z * m;
+                const float w = __shfl_sync(0xffffffffu, wl, lane0 + m);
                 if (s < S) {
-                    const float w = expf(__ldg(pl + s * lse_step) - L);
                     acc.x += w * v[m].x; acc.y += w * v[m].y; acc.z += w * v[m].z; acc.w += w * v[m].w;
                 }
             }

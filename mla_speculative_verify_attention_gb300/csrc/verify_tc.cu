@@ -72,15 +72,16 @@ constexpr int RAW_SCALE = RAW_ROPE + NK * 128;       // bf16 ropes [NK][64], the
 constexpr int RAW_SLOT = RAW_SCALE + NK * 4;         // fp32 scales [NK]: 20608 B
 constexpr int MAX_RAW_SLOTS = 4;
 constexpr uint32_t TMEM_COLS = 512;
-// TMEM columns: S buffers first (bf16 path: two of 32 columns; fp8 path: two pairs
-// of latent / rope scores), then O^T
+// TMEM columns: S buffers first (bf16 path: 32 columns each; fp8 path: latent and rope
+// scores apart, 64), then O^T, then Q chunks.
 template <bool FP8> constexpr int s_cols() { return FP8 ? 2 * NK : NK; }
-// S buffers: the bf16 path double-buffers S so Q K^T of the next tile can run ahead of
-// the softmax; the fp8 path's single issuer reaches Q K^T of tile i + 1 only after P V of
-// tile i - 1, by which time the softmax has long read S of tile i, so one buffer costs it
-// nothing and leaves two more Q chunks' worth of TMEM columns.
-template <bool FP8> constexpr int s_bufs() { return FP8 ? 1 : 2; }
-template <bool FP8> constexpr int o_col0() { return s_bufs<FP8>() * s_cols<FP8>(); }
+// S buffers (SB) and P buffers (PB) per instantiation.  Two S buffers let Q K^T of the
+// next tile run ahead of the softmax; two P buffers let the softmax of tile i write P
+// while P V of tile i - 1 still reads the other.  The fp8 path's single issuer reaches
+// Q K^T of tile i + 1 only after P V of tile i - 1, long after the softmax has read S of
+// tile i, so one S buffer costs it nothing and leaves two more Q chunks' worth of TMEM
+// columns.  The five-stage bf16 variant takes one S and one P buffer: the TMEM columns
+// and shared memory they free hold a fifth Q chunk in TMEM and a fifth key stage.
 constexpr float TAU = 8.0f;                          // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -89,9 +90,10 @@ constexpr float LN2 = 0.6931471805599453f;
 template <int STAGES> struct Bars {
     static constexpr int KV_FULL = 0, KV_EMPTY = STAGES, S_FULL = 2 * STAGES, S_FREE = 2 * STAGES + 2,
                          P_FULL = 2 * STAGES + 4, Q_FULL = 2 * STAGES + 6, QT_FULL = 2 * STAGES + 7,
-                         COUNT = 2 * STAGES + 8;    // P_FULL: one per P buffer
+                         COUNT = 2 * STAGES + 8;    // S_FULL / S_FREE / P_FULL: one per buffer
 };
-static_assert(Bars<3>::COUNT * 8 <= 128 && Bars<4>::COUNT * 8 <= 128, "barrier area");
+constexpr int BAR_BYTES = 256;
+static_assert(Bars<5>::COUNT * 8 <= BAR_BYTES, "barrier area");
 
 struct Layout {
     int q_off, kv_off, p_off, misc_off, total;
@@ -101,21 +103,21 @@ __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a *
 
 // Q: the nq_s shared-memory chunks, regions of R rows x 128 B (MMA rows R..127 read on
 // into the next region and, past the last one, into the key stages: those rows' scores
-// are never used).
-__host__ __device__ inline Layout layout_for(int R, int nq_s, int stages) {
+// are never used).  Then the key stages, the pb P buffers and the small items: barriers,
+// the TMEM address and abort flag, alpha[], 1/l[] and (fp8) the key scales of every stage.
+__host__ __device__ inline Layout layout_for(int R, int nq_s, int stages, int pb, bool fp8) {
     Layout L;
     L.q_off = 0;
     L.kv_off = align_up(nq_s * R * 128, 1024);
     L.p_off = L.kv_off + stages * STAGE_BYTES;
-    L.misc_off = align_up(L.p_off + 2 * R * NK * 2, 128);   // two P buffers
-    L.total = L.misc_off + 128 + 128 + 512 + 512 + stages * NK * 4;  // barriers, tmem slot / flags,
-                                                                     // alpha[], 1/l[], fp8 key scales
+    L.misc_off = align_up(L.p_off + pb * R * NK * 2, 128);
+    L.total = L.misc_off + BAR_BYTES + 128 + 512 + 512 + (fp8 ? stages * NK * 4 : 0);
     return L;
 }
 
-// TMEM columns left for Q chunks (32 columns each) beside the S buffers and O^T.
-__host__ __device__ inline int q_tmem_chunks(bool fp8, int R) {
-    const int used = (fp8 ? s_bufs<true>() * s_cols<true>() : s_bufs<false>() * s_cols<false>()) + 4 * R;
+// TMEM columns left for Q chunks (32 columns each) beside sb S buffers and O^T.
+__host__ __device__ inline int q_tmem_chunks(bool fp8, int R, int sb) {
+    const int used = sb * (fp8 ? s_cols<true>() : s_cols<false>()) + 4 * R;
     const int c = ((int)TMEM_COLS - used) / 32;
     return c < 0 ? 0 : (c > NCHUNK ? NCHUNK : c);
 }
@@ -132,11 +134,11 @@ struct Misc {
 __device__ __forceinline__ Misc misc_at(uint8_t* smem, const Layout& L) {
     Misc m;
     m.bars = reinterpret_cast<uint64_t*>(smem + L.misc_off);
-    m.tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off + 128);
-    m.abort = reinterpret_cast<volatile int*>(smem + L.misc_off + 132);
-    m.alpha = reinterpret_cast<float*>(smem + L.misc_off + 256);
-    m.rinv = reinterpret_cast<float*>(smem + L.misc_off + 768);
-    m.kscale = reinterpret_cast<float*>(smem + L.misc_off + 1280);
+    m.tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off + BAR_BYTES);
+    m.abort = reinterpret_cast<volatile int*>(smem + L.misc_off + BAR_BYTES + 4);
+    m.alpha = reinterpret_cast<float*>(smem + L.misc_off + BAR_BYTES + 128);
+    m.rinv = reinterpret_cast<float*>(smem + L.misc_off + BAR_BYTES + 640);
+    m.kscale = reinterpret_cast<float*>(smem + L.misc_off + BAR_BYTES + 1152);
     return m;
 }
 
@@ -145,25 +147,26 @@ __device__ __forceinline__ void give_up(const Misc& m, unsigned* status) {
 }
 
 
-template <bool FP8, int STAGES, int NQT>
+template <bool FP8, int STAGES, int NQT, int SB, int PB>
 __global__ void __launch_bounds__(NTHREADS, 1)
     verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap q_map, int R, int R_step, int raw_n) {
     constexpr int SC = s_cols<FP8>();
-    constexpr int SB = s_bufs<FP8>();
-    constexpr int O_COL0 = o_col0<FP8>();
+    constexpr int O_COL0 = SB * SC;
     using BR = Bars<STAGES>;
     constexpr int B_KV_FULL = BR::KV_FULL, B_KV_EMPTY = BR::KV_EMPTY, B_S_FULL = BR::S_FULL,
                   B_S_FREE = BR::S_FREE, B_P_FULL = BR::P_FULL, B_Q_FULL = BR::Q_FULL, B_QT_FULL = BR::QT_FULL;
     constexpr int nq_t = NQT;                            // Q chunks 0 .. NQT-1 live in TMEM,
     constexpr int nq_s = NCHUNK - NQT;                   // chunks NQT .. 8 in shared memory
-    constexpr int NQ0 = nq_t < 4 ? nq_t : 4;             // TMEM chunks loaded before the set-up barrier
+    // TMEM chunks loaded before the set-up barrier (an odd count leaves a pair for the loop,
+    // which keeps the register peak of the five-chunk variant below the 168 a thread gets)
+    constexpr int NQ0 = nq_t == 5 ? 3 : (nq_t < 4 ? nq_t : 4);
     const int Q_COL0 = O_COL0 + 4 * R;                   // Q chunk c < nq_t: TMEM columns Q_COL0 + 32 c ..
     extern __shared__ __align__(1024) uint8_t smem[];
     // Launched as a programmatic dependent of the previous kernel on the stream (the KV
     // append, typically): the CTAs become resident while it drains, and wait here until
     // it has completed and its writes are visible, before the first global read.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const Layout L = layout_for(R, nq_s, STAGES);
+    const Layout L = layout_for(R, nq_s, STAGES, PB, FP8);
     const Misc M = misc_at(smem, L);
     const int raw_off = align_up(L.total, 128);          // fp8 path: raw_n raw slots from here
     uint8_t* p_s = smem + L.p_off;
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             bool ok = true;
             if (warp == 1) {
                 for (int j = 0; j < T && ok; ++j) {
-                    ok = mbar_wait(&M.bars[B_P_FULL + (j & 1)], (j >> 1) & 1, M.abort);
+                    ok = mbar_wait(&M.bars[B_P_FULL + j % PB], (j / PB) & 1, M.abort);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         for (int kk = 0; kk < NK / 16; ++kk)
                             mma_bf16(tmem + O_COL0 + ci * R,
                                      dv + st16 + (uint64_t)((2 * ci * REGION + kk * 2048) >> 4),
-                                     dp + (uint64_t)(((j & 1) * R * NK * 2 + kk * 2 * R * 16) >> 4), id_pv,
+                                     dp + (uint64_t)(((j % PB) * R * NK * 2 + kk * 2 * R * 16) >> 4), id_pv,
                                      j > 0 || kk > 0);
                     mma_commit(&M.bars[B_KV_EMPTY + j % STAGES]);
                     }
@@ -383,7 +386,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = ok && mbar_wait(&M.bars[B_QT_FULL], 0, M.abort);
             ok = __all_sync(0xffffffffu, ok);
             auto issue_pv = [&](int j) {
-                ok = ok && mbar_wait(&M.bars[B_P_FULL + (j & 1)], (j >> 1) & 1, M.abort);
+                ok = ok && mbar_wait(&M.bars[B_P_FULL + j % PB], (j / PB) & 1, M.abort);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) return;
                 tc_fence_after();
@@ -395,7 +398,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     for (int kk = 0; kk < NK / 16; ++kk)
                         mma_bf16(tmem + O_COL0 + ci * R,
                                  dv + st16 + (uint64_t)((2 * ci * REGION + kk * 2048) >> 4),
-                                 dp + (uint64_t)(((j & 1) * R * NK * 2 + kk * 2 * R * 16) >> 4), id_pv,
+                                 dp + (uint64_t)(((j % PB) * R * NK * 2 + kk * 2 * R * 16) >> 4), id_pv,
                                  j > 0 || kk > 0);
                 mma_commit(&M.bars[B_KV_EMPTY + j % STAGES]);
                 }
@@ -673,9 +676,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 m = mt;
             }
             const bool any = bar_red_or(1, 128, need);
-            // P buffer i & 1 was last read by P V of tile i - 2; a rescale of O^T also needs
+            // P buffer i % PB was last read by P V of tile i - PB; a rescale of O^T also needs
             // P V of tile i - 1 complete (without one, P V of tiles i - 1 and i commute)
-            if (ok && any && i >= 1)
+            if (ok && (any || PB == 1) && i >= 1)
                 ok = mbar_wait(&M.bars[B_KV_EMPTY + (i - 1) % STAGES], ((i - 1) / STAGES) & 1, M.abort);
             else if (ok && i >= 2)
                 ok = mbar_wait(&M.bars[B_KV_EMPTY + (i - 2) % STAGES], ((i - 2) / STAGES) & 1, M.abort);
@@ -715,12 +718,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // P (B operand, K-major, no swizzle): keys 8 kb .. 8 kb + 7 of row r at kb * (R * 16) + r * 16
 #pragma unroll
                 for (int kb = 0; kb < NK / 8; ++kb)
-                    *reinterpret_cast<uint4*>(p_s + (i & 1) * (R * NK * 2) + kb * (R * 16) + r * 16) =
+                    *reinterpret_cast<uint4*>(p_s + (i % PB) * (R * NK * 2) + kb * (R * 16) + r * 16) =
                         make_uint4(pk[4 * kb], pk[4 * kb + 1], pk[4 * kb + 2], pk[4 * kb + 3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&M.bars[B_P_FULL + (i & 1)]);
+            mbar_arrive(&M.bars[B_P_FULL + i % PB]);
         }
         if (ok && T > 0) ok = mbar_wait(&M.bars[B_KV_EMPTY + (T - 1) % STAGES], ((T - 1) / STAGES) & 1, M.abort);
         const bool failed = bar_red_or(1, 128, !ok);
@@ -790,19 +793,20 @@ void tc_tiling(int rows, int max_r, int* n_tiles, int* R_step, int* R) {
 namespace {
 constexpr int MAX_SMEM = 232448;                     // opt-in shared memory per block on sm_103
 
-// Instantiations: (fp8, key stages, Q chunks in TMEM).  q_tmem_chunks gives 4 for up to
-// 80 rows on the bf16 path, 2 beyond that; the fp8 path (one S buffer) takes 6 up to 64
-// rows and 4 at 80.  Four bf16 stages fit whenever four or more chunks leave shared
-// memory; the fp8 path keeps three so that two to four raw slots fit beside them.
-template <bool FP8, int STAGES, int NQT>
+// Instantiations: (fp8, key stages, Q chunks in TMEM, S buffers, P buffers).  bf16 up to
+// 80 rows: five stages with one S and one P buffer and five Q chunks in TMEM; at 96 rows
+// three stages, two chunks in TMEM.  fp8 (one S buffer): six chunks up to 64 rows, four
+// at 80, three bf16 stages so that two to four raw slots fit beside them.
+template <bool FP8, int STAGES, int NQT, int SB, int PB>
 cudaError_t launch_one(bool set_attr, dim3 grid, cudaStream_t stream, const VerifyArgs& a, const CUtensorMap& q_map,
                        int R, int R_step) {
-    auto* k = verify_tc_kernel<FP8, STAGES, NQT>;
+    auto* k = verify_tc_kernel<FP8, STAGES, NQT, SB, PB>;
     if (set_attr) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SMEM);
         if (e != cudaSuccess) return e;
     }
-    int smem = layout_for(R, NCHUNK - NQT, STAGES).total;
+    if (q_tmem_chunks(FP8, R, SB) < NQT) return cudaErrorInvalidConfiguration;
+    int smem = layout_for(R, NCHUNK - NQT, STAGES, PB, FP8).total;
     int raw_n = 0;
     if (FP8) {                                       // as many raw slots as still fit
         smem = align_up(smem, 128);
@@ -840,9 +844,6 @@ cudaError_t launch_verify_tc(const VerifyArgs& a_in, cudaStream_t stream) {
     // fp8: at 96 rows no TMEM is left for Q and the shared-memory Q tile, the key stages
     // and two P buffers exceed the opt-in limit, so its tiles stop at 80 rows
     tc_tiling(a.q_len * a.H, a.kv_fp8 ? 80 : MAX_R, &n_tiles, &R_step, &R);
-    const int qt = q_tmem_chunks(a.kv_fp8, R);
-    const int nq = a.kv_fp8 ? (qt >= 6 ? 6 : qt >= 4 ? 4 : 0) : (qt >= 4 ? 4 : qt >= 2 ? 2 : 0);
-    const bool four = layout_for(R, NCHUNK - nq, 4).total <= MAX_SMEM;
     CUtensorMap q_map;
     const uint64_t q_rows = (uint64_t)a.B * a.q_len * a.H;
     if (!encode_bf16_2d_sw128(&q_map, a.q, D_QK, q_rows, D_QK * 2, 64, (uint32_t)R,
@@ -850,17 +851,15 @@ cudaError_t launch_verify_tc(const VerifyArgs& a_in, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     dim3 grid(a.nsplit, n_tiles, a.balanced ? 1 : a.B);
     int which;
-    if (!a.kv_fp8) which = nq == 4 ? 0 : 1;
-    else which = nq == 6 ? 2 : nq == 4 ? 3 : 4;
+    if (!a.kv_fp8) which = R <= 80 ? 0 : 1;
+    else which = q_tmem_chunks(true, R, 1) >= 6 ? 2 : 3;
     const bool set = !attr_set[dev][which];
     switch (which) {
-        case 0: e = four ? launch_one<false, 4, 4>(set, grid, stream, a, q_map, R, R_step)
-                         : cudaErrorInvalidConfiguration; break;
-        case 1: e = four ? cudaErrorInvalidConfiguration
-                         : launch_one<false, 3, 2>(set, grid, stream, a, q_map, R, R_step); break;
-        case 2: e = launch_one<true, 3, 6>(set, grid, stream, a, q_map, R, R_step); break;
-        case 3: e = launch_one<true, 3, 4>(set, grid, stream, a, q_map, R, R_step); break;
-        default: e = cudaErrorInvalidConfiguration; break;   // unreachable: fp8 tiles stop at 80 rows
+        case 0: e = launch_one<false, 5, 5, 1, 1>(set, grid, stream, a, q_map, R, R_step); break;
+        case 1: e = launch_one<false, 3, 2, 2, 2>(set, grid, stream, a, q_map, R, R_step); break;
+        case 2: e = launch_one<true, 3, 6, 1, 2>(set, grid, stream, a, q_map, R, R_step); break;
+        case 3: e = launch_one<true, 3, 4, 1, 2>(set, grid, stream, a, q_map, R, R_step); break;
+        default: e = cudaErrorInvalidConfiguration; break;
     }
     if (e == cudaSuccess) attr_set[dev][which] = true;
     return e;

@@ -61,8 +61,11 @@ using namespace tc;
 
 constexpr int NK = 32;                               // keys per tile
 constexpr int MAX_R = 96;                            // query rows per CTA
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 320;                        // bf16 path: ten warps
 constexpr int GATHER_WARPS = 4;
+// fp8 path: two more warps (10, 11) copy the raw rows, so warps 6-9 only widen.  Twelve
+// warps still give a thread the 168 registers of three warps per SM sub-partition.
+template <bool FP8> constexpr int block_threads() { return FP8 ? NTHREADS + 64 : NTHREADS; }
 constexpr int NCHUNK = D_QK / 64;                    // 9 swizzled 64-dim regions per row
 constexpr int REGION = NK * 128;                     // one 64-dim region of a stage: 4096 B
 constexpr int STAGE_BYTES = NCHUNK * REGION;         // 36864 B
@@ -90,7 +93,8 @@ constexpr float LN2 = 0.6931471805599453f;
 template <int STAGES> struct Bars {
     static constexpr int KV_FULL = 0, KV_EMPTY = STAGES, S_FULL = 2 * STAGES, S_FREE = 2 * STAGES + 2,
                          P_FULL = 2 * STAGES + 4, Q_FULL = 2 * STAGES + 6, QT_FULL = 2 * STAGES + 7,
-                         COUNT = 2 * STAGES + 8;    // S_FULL / S_FREE / P_FULL: one per buffer
+                         RAW_FULL = 2 * STAGES + 8, RAW_EMPTY = 2 * STAGES + 12,   // fp8 raw slots
+                         COUNT = 2 * STAGES + 16;   // S_FULL / S_FREE / P_FULL: one per buffer
 };
 constexpr int BAR_BYTES = 256;
 static_assert(Bars<5>::COUNT * 8 <= BAR_BYTES, "barrier area");
@@ -148,13 +152,15 @@ __device__ __forceinline__ void give_up(const Misc& m, unsigned* status) {
 
 
 template <bool FP8, int STAGES, int NQT, int SB, int PB>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(block_threads<FP8>(), 1)
     verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap q_map, int R, int R_step, int raw_n) {
+    constexpr int NT = block_threads<FP8>();
     constexpr int SC = s_cols<FP8>();
     constexpr int O_COL0 = SB * SC;
     using BR = Bars<STAGES>;
     constexpr int B_KV_FULL = BR::KV_FULL, B_KV_EMPTY = BR::KV_EMPTY, B_S_FULL = BR::S_FULL,
-                  B_S_FREE = BR::S_FREE, B_P_FULL = BR::P_FULL, B_Q_FULL = BR::Q_FULL, B_QT_FULL = BR::QT_FULL;
+                  B_S_FREE = BR::S_FREE, B_P_FULL = BR::P_FULL, B_Q_FULL = BR::Q_FULL, B_QT_FULL = BR::QT_FULL,
+                  B_RAW_FULL = BR::RAW_FULL, B_RAW_EMPTY = BR::RAW_EMPTY;
     constexpr int nq_t = NQT;                            // Q chunks 0 .. NQT-1 live in TMEM,
     constexpr int nq_s = NCHUNK - NQT;                   // chunks NQT .. 8 in shared memory
     // TMEM chunks loaded before the set-up barrier (an odd count leaves a pair for the loop,
@@ -260,12 +266,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mbar_init(&M.bars[B_KV_FULL + i], 32 * GATHER_WARPS);
                 mbar_init(&M.bars[B_KV_EMPTY + i], 1);
             }
+            if (FP8)
+                for (int i = 0; i < MAX_RAW_SLOTS; ++i) {
+                    mbar_init(&M.bars[B_RAW_FULL + i], 64);   // the copy warps' cp.async arrivals
+                    mbar_init(&M.bars[B_RAW_EMPTY + i], GATHER_WARPS);
+                }
             *M.abort = misaligned ? 1 : 0;
             mbar_init_fence();
         }
         __syncwarp();
-        bar_sync(4, 32 * GATHER_WARPS);                  // the gather warps see their barriers
-        bar_arrive(3, NTHREADS);
+        bar_sync(4, NT - 32 * 6);                        // the gather warps see their barriers
+        bar_arrive(3, NT);
     } else if (!misaligned && nq_t > 0) {
         // the first TMEM chunks of Q row r (rows past the tile: zeros)
         const int r = (warp & 3) * 32 + lane;
@@ -277,12 +288,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp < 6) {
         tc_fence_before();
         __syncwarp();
-        bar_sync(3, NTHREADS);
+        bar_sync(3, NT);
         tc_fence_after();
     }
     const uint32_t tmem = warp < 6 ? *M.tmem_slot : 0u;
 
-    if (!FP8 && warp <= 1) {
+    if (warp <= 1) {
         // ================= MMA issue, bf16: warp 0 Q K^T, warp 1 P V =================
         // Two issuers: Q K^T of tile i goes out as soon as its keys and S buffer are ready,
         // P V of tile j as soon as its P is written, so a key stage is released right after
@@ -362,7 +373,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             if (!ok && lane == 0) give_up(M, a.status);
-        } else if (warp == 1 && !misaligned) {
+        } else if (warp == 1 && !misaligned && !FP8) {
             mbar_wait(&M.bars[B_Q_FULL], 0, M.abort);   // no keys: the Q copies must land before exit
         }
         __syncwarp();
@@ -458,7 +469,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             return __ldg(slot_row + j);
         };
         int cur = spec_cur, nxt = spec_nxt;
-        if (!spec_ok) {
+        if (!FP8 && !spec_ok) {
             cur = load_slots(0);
             nxt = load_slots(4);
         }
@@ -495,50 +506,70 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 if (!(a.debug_stall && i == 0)) cp_async_arrive_noinc(&M.bars[B_KV_FULL + st]);
             }
-        } else {
-            // The raw rows (e4m3 latent, bf16 rope, fp32 scale) are copied raw_n - 1 tiles
-            // ahead into a ring of raw slots, so several tiles' reads are in flight; each
-            // warp then widens its own 8 keys into the swizzled bf16 stage.  Group k of
-            // every thread's cp.async groups holds tile k (or nothing past the last tile).
+        } else if (warp >= 10) {
+            // ---- fp8 raw copies: warp 10 + c copies keys 16 c .. 16 c + 15 of every tile (e4m3
+            // latent, bf16 rope, fp32 scale) into the ring of raw_n raw slots, up to raw_n tiles
+            // ahead of the widening warps; a slot is refilled once all four widening warps have
+            // read it.  Arrivals are asynchronous (cp.async.mbarrier.arrive), so this warp
+            // moves on while its copies are in flight.
+            const int c = warp - 10;
             const uint32_t raw_addr = smem_u32(smem + raw_off);
-            auto copy_raw = [&](int j) {
-                const int sl = next_slots(j);
-                const uint32_t rb = raw_addr + (uint32_t)((j % raw_n) * RAW_SLOT);
+            // slot indices two tiles per load: lane l holds key 16 c + (l & 15) of tile t0 + (l >> 4)
+            auto load2 = [&](int t0) -> int {
+                const int t = t0 + (lane >> 4);
+                if (t >= T) return 0;
+                const int j = min(k_begin + t * NK + 16 * c + (lane & 15), k_end - 1);   // past the split: a valid key
+                return __ldg(slot_row + j);
+            };
+            cur = load2(0);
+            nxt = load2(2);
+            for (int j = 0; j < T; ++j) {
+                if ((j & 1) == 0) {
+                    if (j > 0) {
+                        cur = nxt;
+                        nxt = load2(j + 2);
+                    }
+                    if (cur < 0 || (int64_t)cur >= a.n_pool) { bad_slot = true; cur = 0; }
+                }
+                const int sl = __shfl_sync(0xffffffffu, cur, ((j & 1) << 4) + (lane & 15));   // key 16 c + (lane & 15)
+                const int rs = j % raw_n;
+                if (j >= raw_n && !mbar_wait(&M.bars[B_RAW_EMPTY + rs], ((j - raw_n) / raw_n) & 1, M.abort)) {
+                    give_up(M, a.status);
+                    break;
+                }
+                const uint32_t rb = raw_addr + (uint32_t)(rs * RAW_SLOT);
 #pragma unroll
-                for (int it = 0; it < 8; ++it) {         // latent: one 512-byte row per step
+                for (int it = 0; it < 16; ++it) {        // latent: one 512-byte row per step
                     const int row_slot = __shfl_sync(0xffffffffu, sl, it);
-                    cp_async16(rb + (8 * w + it) * D_V + lane * 16, a.kv_lat + (int64_t)row_slot * D_V + lane * 16);
+                    cp_async16(rb + (16 * c + it) * D_V + lane * 16, a.kv_lat + (int64_t)row_slot * D_V + lane * 16);
                 }
 #pragma unroll
-                for (int it = 0; it < 2; ++it) {         // rope: 8 rows x 8 pieces of 16 bytes
+                for (int it = 0; it < 4; ++it) {         // rope: 16 rows x 8 pieces of 16 bytes
                     const int f = it * 32 + lane;
                     const int row_slot = __shfl_sync(0xffffffffu, sl, f >> 3);
-                    cp_async16(rb + RAW_ROPE + (8 * w + (f >> 3)) * 128 + (f & 7) * 16,
+                    cp_async16(rb + RAW_ROPE + (16 * c + (f >> 3)) * 128 + (f & 7) * 16,
                                a.kv_rope + (int64_t)row_slot * 64 + (f & 7) * 8);
                 }
-                if (lane < 8) cp_async4(rb + RAW_SCALE + (8 * w + lane) * 4, a.kv_scale + sl);
-            };
-            for (int j = 0; j < raw_n - 1; ++j) {
-                if (j < T) copy_raw(j);
-                cp_async_commit();
+                if (lane < 16) cp_async4(rb + RAW_SCALE + (16 * c + lane) * 4, a.kv_scale + sl);
+                cp_async_arrive_noinc(&M.bars[B_RAW_FULL + rs]);
             }
-            // lane l widens dims 16 l .. 16 l + 15: 16-byte pieces j0, j0 + 1 of region l / 4.
-            // Lanes of odd regions store their second piece first, so each store covers all
-            // eight 16-byte bank groups (four lanes each) instead of four.
+        } else {
+            // ---- fp8 widening: warp 6 + w widens keys 8 w .. 8 w + 7 of every tile from its raw
+            // slot into the swizzled bf16 stage layout.  lane l widens dims 16 l .. 16 l + 15:
+            // 16-byte pieces j0, j0 + 1 of region l / 4.  Lanes of odd regions store their second
+            // piece first, so each store covers all eight 16-byte bank groups (four lanes each)
+            // instead of four.
             const int region = lane >> 2, j0 = (lane & 3) * 2, odd = region & 1;
             for (int i = 0; i < T; ++i) {
-                const int st = i % STAGES;
-                if (i + raw_n - 1 < T) copy_raw(i + raw_n - 1);   // into the slot tile i - 1 used
-                cp_async_commit();
-                cp_async_wait_pending(raw_n - 1);                 // tile i has landed (this thread)
-                __syncwarp();                                     // ... for the whole warp
-                if (i >= STAGES && !mbar_wait(&M.bars[B_KV_EMPTY + st], ((i - STAGES) / STAGES) & 1, M.abort)) {
+                const int st = i % STAGES, rs = i % raw_n;
+                if (!mbar_wait(&M.bars[B_RAW_FULL + rs], (i / raw_n) & 1, M.abort) ||
+                    (i >= STAGES && !mbar_wait(&M.bars[B_KV_EMPTY + st], ((i - STAGES) / STAGES) & 1, M.abort))) {
                     give_up(M, a.status);
                     break;
                 }
                 // All reads of the raw slot first: the compiler cannot tell the raw slot from
                 // the stage it writes, so reads placed after a store would wait for it.
-                const uint8_t* rb = smem + raw_off + (i % raw_n) * RAW_SLOT;
+                const uint8_t* rb = smem + raw_off + rs * RAW_SLOT;
                 uint4 raw[8], rope[2];
 #pragma unroll
                 for (int it = 0; it < 8; ++it)
@@ -563,13 +594,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int it = 0; it < 2; ++it) {
                     const int f = it * 32 + lane;
-                    const int key = 8 * w + (f >> 3), c = f & 7;
-                    *reinterpret_cast<uint4*>(sbase + 8 * REGION + key * 128 + ((c ^ (key & 7)) << 4)) = rope[it];
+                    const int key = 8 * w + (f >> 3), cc = f & 7;
+                    *reinterpret_cast<uint4*>(sbase + 8 * REGION + key * 128 + ((cc ^ (key & 7)) << 4)) = rope[it];
                 }
                 if (lane < 8) M.kscale[st * NK + 8 * w + lane] = ksc;
                 fence_proxy_async_smem();                         // generic stores -> tensor-core reads
                 if (!(a.debug_stall && i == 0)) mbar_arrive(&M.bars[B_KV_FULL + st]);
-                __syncwarp();                                     // raw slot read before it is refilled
+                __syncwarp();                                     // raw slot read by the whole warp
+                if (lane == 0) mbar_arrive(&M.bars[B_RAW_EMPTY + rs]);
             }
         }
         cp_async_wait_all();
@@ -639,11 +671,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tmem_ld_wait();
                 // the key scales were written before the tile's kv_full arrival
                 ok = mbar_wait(&M.bars[B_KV_FULL + i % STAGES], (i / STAGES) & 1, M.abort);
+                const float4* ks4 = reinterpret_cast<const float4*>(M.kscale + (i % STAGES) * NK);
 #pragma unroll
-                for (int k = 0; k < NK; ++k) {
-                    ksc[k] = M.kscale[(i % STAGES) * NK + k];
-                    sv[k] = __float_as_uint(ksc[k] * __uint_as_float(sv[k]) + __uint_as_float(sr[k]));
+                for (int k4 = 0; k4 < NK / 4; ++k4) {
+                    const float4 v = ks4[k4];
+                    ksc[4 * k4] = v.x; ksc[4 * k4 + 1] = v.y; ksc[4 * k4 + 2] = v.z; ksc[4 * k4 + 3] = v.w;
                 }
+#pragma unroll
+                for (int k = 0; k < NK; ++k)
+                    sv[k] = __float_as_uint(ksc[k] * __uint_as_float(sv[k]) + __uint_as_float(sr[k]));
             } else {
                 tmem_ld_wait();
             }
@@ -818,7 +854,7 @@ cudaError_t launch_one(bool set_attr, dim3 grid, cudaStream_t stream, const Veri
     if (smem > MAX_SMEM) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(NTHREADS);
+    cfg.blockDim = dim3(block_threads<FP8>());
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -46,6 +46,21 @@ def test_balanced_parity(cuda_lib, B, H, prefixes):
     compare(out_u, lse_u, ro, rl, what=f"uniform B{B} H{H}")
 
 
+@pytest.mark.parametrize("B", [65, 128])
+def test_many_streams_parity(cuda_lib, B):
+    """More streams than the balanced split takes (64): the automatic split count falls back
+    to the uniform per-stream split over two waves; mixed lengths U{256..4096} (a serving
+    batch of 128 streams) must still match the oracle."""
+    mv = cuda_lib
+    prefixes = w.mixed_prefixes(7, B, 256, 4096)
+    inp = w.make_verify("many", B, 9, 8, prefixes, seed=120 + B, scattered=True, mask_kind="tree",
+                        n_pool=sum(prefixes) + 9 * B + 4096)
+    out, lse = _run(mv, inp)
+    ro, rl = oracle.verify_inputs(inp)
+    compare(out, lse, ro, rl, what=f"{B} streams")
+    assert mv.device_status() == 0
+
+
 def test_balanced_bad_length_stream(cuda_lib):
     mv = cuda_lib
     inp = w.make_verify("balbad", 4, 9, 8, [2000, 300, 0, 5000], seed=110, scattered=True, mask_kind="tree",

@@ -7,40 +7,44 @@
 //            stage; arrivals are asynchronous, so a warp moves on to the next tile
 //            while its copies are in flight (measured on GB300: random 1152-byte
 //            rows gather about twice as fast this way as with TMA tile::gather4,
-//            whose per-instruction cost caps a 512-byte gather).  fp8 keys: the raw
-//            rows (e4m3 latent, bf16 rope, fp32 scale) go by cp.async into a ring of
-//            raw slots a few tiles ahead, and each warp widens its keys into the
-//            same bf16 stage layout
+//            whose per-instruction cost caps a 512-byte gather).  fp8 keys: two more
+//            warps copy the raw rows (e4m3 latent, bf16 rope, fp32 scale) by cp.async
+//            into a ring of raw slots up to a few tiles ahead, and the four gather
+//            warps widen them into the same bf16 stage layout
 //   S        = Q K^T: tcgen05.mma M=128 (query rows) x N=32 (keys) x K=576, fp32 in TMEM;
 //            the first 64-dim chunks of Q sit in TMEM (A operand read from tensor
 //            memory, no shared-memory traffic), the rest in shared memory
 //   P        = softmax(S): one thread per query row reads its S row from TMEM, applies
 //            the draft mask, keeps a running max / sum (online softmax) and writes
-//            P (bf16) to one of two shared-memory buffers; it waits for P V of the
-//            previous tile only when the running max moved enough to rescale O^T, so
-//            softmax of tile i overlaps P V of tile i - 1
+//            P (bf16) to a shared-memory buffer; it waits for P V of the previous tile
+//            only when the running max moved enough to rescale O^T or when P has one
+//            buffer, so softmax of tile i otherwise overlaps P V of tile i - 1
 //   O^T     += V^T P^T: tcgen05.mma M=128 (value dims) x N=rows x K=32 (keys), four
 //            128-dim chunks, fp32 accumulators resident in TMEM
 // Computing P V transposed keeps O^T in 4 x rows <= 384 TMEM columns, so the S
 // buffers fit beside it in the 512-column TMEM and Q K^T runs once per tile (bf16:
-// two S buffers of 32 columns; fp8: one of 64, latent and rope scores apart); the
-// columns left over hold as many 32-column Q chunks as fit (bf16: 4 for up to 80
-// rows; fp8: 6 for up to 64).  Measured on GB300, an M=128 x N=32 x K=16 MMA issued from a
-// converged warp takes ~17 cycles with A in TMEM and ~40 with A in shared memory
-// (bound by shared-memory reads of the 4 KB A tile), so every Q chunk moved to TMEM
-// takes four MMAs off the shared-memory port, and the freed shared memory buys a
-// fourth key stage.  The same swizzled key stage is the K-major B operand of Q K^T
-// and the M-major A operand of V^T P^T (V = first 512 dims of each key row).
+// one or two S buffers of 32 columns; fp8: one of 64, latent and rope scores apart);
+// the columns left over hold as many 32-column Q chunks as fit (bf16: 5 up to 80 rows
+// with one S buffer, 2 at 96 with two; fp8: 6 up to 64 rows).  Measured on GB300, an
+// M=128 x N=32 x K=16 MMA issued from a converged warp takes ~17 cycles with A in TMEM
+// and ~40 with A in shared memory (bound by shared-memory reads of the 4 KB A tile),
+// so every Q chunk moved to TMEM takes four MMAs off the shared-memory port, and the
+// freed shared memory buys key stages: five for up to 80 bf16 rows (one P buffer),
+// three at 96 rows and on the fp8 path.  The same swizzled key stage is the K-major B
+// operand of Q K^T and the M-major A operand of V^T P^T (V = first 512 dims of each key
+// row).
 //
-// Warp roles (320 threads):
+// Warp roles (320 threads; 384 on the fp8 path):
 //   warp 0      TMEM allocation; Q K^T issue loop run by the whole warp (operands stay
-//               warp-uniform), one elected lane issuing each MMA and commit (fp8: P V too)
+//               warp-uniform), one elected lane issuing each MMA and commit
 //   warp 1      TMA copies of the shared-memory part of the Q tile (64-dim boxes of R
-//               rows), then (bf16) the P V issue loop in the same style
+//               rows), then the P V issue loop in the same style
 //   warps 2-5   Q chunks into TMEM (thread = query row), softmax (thread = query row =
 //               TMEM lane) and the epilogue (thread = value dim = TMEM lane of O^T);
 //               TMEM lane quadrant = warp % 4
-//   warps 6-9   key-tile gather into a 3- or 4-stage ring; warp 6 + w copies keys 8w .. 8w+7
+//   warps 6-9   key-tile gather into the stage ring (bf16) or widening of the raw rows
+//               (fp8); warp 6 + w handles keys 8w .. 8w+7
+//   warps 10-11 fp8 only: raw-row copies, warp 10 + c keys 16c .. 16c+15
 // Every role initialises its own mbarriers and starts its first cold reads (Q, slot
 // indices, key rows) before the block-wide set-up barrier, which the gather warps only
 // arrive at.
@@ -294,13 +298,12 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
     const uint32_t tmem = warp < 6 ? *M.tmem_slot : 0u;
 
     if (warp <= 1) {
-        // ================= MMA issue, bf16: warp 0 Q K^T, warp 1 P V =================
+        // ================= MMA issue: warp 0 Q K^T, warp 1 P V =================
         // Two issuers: Q K^T of tile i goes out as soon as its keys and S buffer are ready,
         // P V of tile j as soon as its P is written, so a key stage is released right after
         // its P V instead of after the next tile's Q K^T (measured on GB300: c4 -7%,
-        // c3-64k -5%).  They write different TMEM columns (S buffers / O^T) and only read
-        // shared memory; each commit tracks its own thread's MMAs.  The fp8 path keeps one
-        // issuer (P V of tile i - 1 after Q K^T of tile i): split issue measured slower there.
+        // c3-64k -5%; fp8 c5 -1.3 us).  They write different TMEM columns (S buffers /
+        // O^T) and only read shared memory; each commit tracks its own thread's MMAs.
         if (T > 0) {
             const uint32_t id_qk = idesc_bf16(128, NK, false, false);
             const uint32_t id_pv = idesc_bf16(128, R, true, false);
@@ -377,82 +380,6 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
             mbar_wait(&M.bars[B_Q_FULL], 0, M.abort);   // no keys: the Q copies must land before exit
         }
         __syncwarp();
-    } else if (FP8 && warp == 0) {
-        // ================= MMA issue, fp8: warp 0 issues Q K^T and P V =================
-        if (T > 0) {
-            const uint32_t id_qk = idesc_bf16(128, NK, false, false);
-            const uint32_t id_pv = idesc_bf16(128, R, true, false);
-            // Q (shared-memory chunks): K-major, 128-byte swizzle, 8-row groups 1024 B apart;
-            // a 16-dim step moves 32 B inside the 128-byte rows, a 64-dim step moves to the
-            // next region (R * 128 B)
-            const uint64_t dq = smem_desc_sw128(q_addr, 16, 1024);
-            // key stage: the same layout with 32-row regions (REGION bytes)
-            const uint64_t dk = smem_desc_sw128(kv_addr, 16, 1024);
-            // V^T: M-major, 64-dim chunks REGION apart, 8-key groups 1024 B apart
-            const uint64_t dv = smem_desc_sw128(kv_addr, REGION, 1024);
-            // P: K-major, no swizzle, 8-key blocks R * 16 B apart, 8-row blocks 128 B apart
-            const uint64_t dp = smem_desc(p_addr, R * 16, 128);
-            const uint32_t q_region16 = (uint32_t)(R * 128) >> 4;
-            bool ok = mbar_wait(&M.bars[B_Q_FULL], 0, M.abort);
-            ok = ok && mbar_wait(&M.bars[B_QT_FULL], 0, M.abort);
-            ok = __all_sync(0xffffffffu, ok);
-            auto issue_pv = [&](int j) {
-                ok = ok && mbar_wait(&M.bars[B_P_FULL + j % PB], (j / PB) & 1, M.abort);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) return;
-                tc_fence_after();
-                const uint64_t st16 = (uint64_t)((j % STAGES) * STAGE_BYTES) >> 4;
-                if (elect_one()) {
-#pragma unroll
-                for (int ci = 0; ci < 4; ++ci)
-#pragma unroll
-                    for (int kk = 0; kk < NK / 16; ++kk)
-                        mma_bf16(tmem + O_COL0 + ci * R,
-                                 dv + st16 + (uint64_t)((2 * ci * REGION + kk * 2048) >> 4),
-                                 dp + (uint64_t)(((j % PB) * R * NK * 2 + kk * 2 * R * 16) >> 4), id_pv,
-                                 j > 0 || kk > 0);
-                mma_commit(&M.bars[B_KV_EMPTY + j % STAGES]);
-                }
-                __syncwarp();
-            };
-            for (int i = 0; i < T && ok; ++i) {
-                const int st = i % STAGES;
-                ok = mbar_wait(&M.bars[B_KV_FULL + st], (i / STAGES) & 1, M.abort);
-                if (ok && i >= SB) ok = mbar_wait(&M.bars[B_S_FREE + i % SB], ((i - SB) / SB) & 1, M.abort);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                fence_proxy_async_smem();              // cp.async (generic proxy) data -> tensor-core reads
-                tc_fence_after();
-                const uint64_t st16 = (uint64_t)(st * STAGE_BYTES) >> 4;
-                const uint32_t d_s = tmem + (i % SB) * SC;
-                if (elect_one()) {
-#pragma unroll
-                for (int ks = 0; ks < D_QK / 16; ++ks) {
-                    const int c = ks >> 2;
-                    const uint32_t ko = (uint32_t)((c * REGION + (ks & 3) * 32) >> 4);
-                    // fp8 path: latent dims (ks < 32) and rope dims accumulate separately, so
-                    // the per-key scale can multiply the latent part alone
-                    const bool rope = FP8 && ks >= D_V / 16;
-                    const uint32_t d = rope ? d_s + NK : d_s;
-                    const bool acc = rope ? ks > D_V / 16 : ks > 0;
-                    if (c < nq_t) {
-                        mma_bf16_ta(d, tmem + Q_COL0 + ks * 8, dk + st16 + ko, id_qk, acc);
-                    } else {
-                        const uint32_t qo = (uint32_t)(c - nq_t) * q_region16 + (uint32_t)(ks & 3) * 2;
-                        mma_bf16(d, dq + qo, dk + st16 + ko, id_qk, acc);
-                    }
-                }
-                mma_commit(&M.bars[B_S_FULL + i % SB]);
-                }
-                __syncwarp();
-                if (i >= 1) issue_pv(i - 1);
-            }
-            if (ok) issue_pv(T - 1);
-            if (!ok && lane == 0) give_up(M, a.status);
-        }
-        __syncwarp();
-    } else if (FP8 && warp == 1) {
-        // Q tile copies were issued during set-up
     } else if (warp >= 6) {
         // ================= key-tile gather: keys 8w .. 8w+7 of every tile =================
         const int w = warp - 6;

@@ -259,13 +259,13 @@ int mla_sparse_fp8_partials(const void* q, const uint8_t* kv_lat_e4m3, const flo
  * explicit nsplit whose partials need more than MLA_STATIC_SCRATCH_BYTES
  * (mla_verify_workspace_bytes) returns MLA_ERR_WORKSPACE.
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  The address is cached per device ordinal for the device's
- * primary context (the CUDA runtime's context): the entry point supports that
- * context only, and must not be used again after cudaDeviceReset.  All calls on a device share the one array and it keeps
- * the last call's contents (every call overwrites what it reads, so nothing
- * needs clearing); calls whose GPU work overlaps -- on different streams, or
- * from different host threads -- race on it and must be serialised by the caller.
+ * (cudaGetSymbolAddress) with that device current.  The address is cached per
+ * device ordinal for the device's primary context (the CUDA runtime's context):
+ * the entry point supports that context only, and must not be used again after
+ * cudaDeviceReset.  All calls on a device share the one array and it keeps the
+ * last call's contents (every call overwrites what it reads, so nothing needs
+ * clearing); calls whose GPU work overlaps -- on different streams, or from
+ * different host threads -- race on it and must be serialised by the caller.
  */
 #define MLA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 int mla_verify_attn_static_scratch(const void* q, const void* kv_cache, int64_t n_pool,

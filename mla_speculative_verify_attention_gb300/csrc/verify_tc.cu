@@ -10,7 +10,10 @@
 //            whose per-instruction cost caps a 512-byte gather).  fp8 keys: two more
 //            warps copy the raw rows (e4m3 latent, bf16 rope, fp32 scale) by cp.async
 //            into a ring of raw slots up to a few tiles ahead, and the four gather
-//            warps widen them into the same bf16 stage layout
+//            warps widen them into the same bf16 stage layout, each latent value
+//            multiplied by its key's scale (bf16(scale_t * code), relative error at
+//            most 2^-8; the rope dims are bf16 already), so from there on both paths
+//            are the same
 //   S        = Q K^T: tcgen05.mma M=128 (query rows) x N=32 (keys) x K=576, fp32 in TMEM;
 //            the first 64-dim chunks of Q sit in TMEM (A operand read from tensor
 //            memory, no shared-memory traffic), the rest in shared memory
@@ -22,10 +25,9 @@
 //   O^T     += V^T P^T: tcgen05.mma M=128 (value dims) x N=rows x K=32 (keys), four
 //            128-dim chunks, fp32 accumulators resident in TMEM
 // Computing P V transposed keeps O^T in 4 x rows <= 384 TMEM columns, so the S
-// buffers fit beside it in the 512-column TMEM and Q K^T runs once per tile (bf16:
-// one or two S buffers of 32 columns; fp8: one of 64, latent and rope scores apart);
-// the columns left over hold as many 32-column Q chunks as fit (bf16: 5 up to 80 rows
-// with one S buffer, 2 at 96 with two; fp8: 6 up to 64 rows).  Measured on GB300, an
+// buffers (one or two of 32 columns) fit beside it in the 512-column TMEM and Q K^T
+// runs once per tile; the columns left over hold as many 32-column Q chunks as fit (5
+// up to 80 rows with one S buffer, 2 at 96 with two, 7 up to 64 rows).  Measured on GB300, an
 // M=128 x N=32 x K=16 MMA issued from a converged warp takes ~17 cycles with A in TMEM
 // and ~40 with A in shared memory (bound by shared-memory reads of the 4 KB A tile),
 // so every Q chunk moved to TMEM takes four MMAs off the shared-memory port, and the
@@ -79,16 +81,13 @@ constexpr int RAW_SCALE = RAW_ROPE + NK * 128;       // bf16 ropes [NK][64], the
 constexpr int RAW_SLOT = RAW_SCALE + NK * 4;         // fp32 scales [NK]: 20608 B
 constexpr int MAX_RAW_SLOTS = 4;
 constexpr uint32_t TMEM_COLS = 512;
-// TMEM columns: S buffers first (bf16 path: 32 columns each; fp8 path: latent and rope
-// scores apart, 64), then O^T, then Q chunks.
-template <bool FP8> constexpr int s_cols() { return FP8 ? 2 * NK : NK; }
+// TMEM columns: S buffers first (32 columns each), then O^T, then Q chunks.
 // S buffers (SB) and P buffers (PB) per instantiation.  Two S buffers let Q K^T of the
 // next tile run ahead of the softmax; two P buffers let the softmax of tile i write P
-// while P V of tile i - 1 still reads the other.  The fp8 path's single issuer reaches
-// Q K^T of tile i + 1 only after P V of tile i - 1, long after the softmax has read S of
-// tile i, so one S buffer costs it nothing and leaves two more Q chunks' worth of TMEM
-// columns.  The five-stage bf16 variant takes one S and one P buffer: the TMEM columns
-// and shared memory they free hold a fifth Q chunk in TMEM and a fifth key stage.
+// while P V of tile i - 1 still reads the other.  One S buffer leaves a Q chunk's worth
+// more of TMEM columns.  The five-stage bf16 variant takes one S and one P buffer: the
+// TMEM columns and shared memory they free hold a fifth Q chunk in TMEM and a fifth key
+// stage.
 constexpr float TAU = 8.0f;                          // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -112,20 +111,20 @@ __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a *
 // Q: the nq_s shared-memory chunks, regions of R rows x 128 B (MMA rows R..127 read on
 // into the next region and, past the last one, into the key stages: those rows' scores
 // are never used).  Then the key stages, the pb P buffers and the small items: barriers,
-// the TMEM address and abort flag, alpha[], 1/l[] and (fp8) the key scales of every stage.
-__host__ __device__ inline Layout layout_for(int R, int nq_s, int stages, int pb, bool fp8) {
+// the TMEM address and abort flag, alpha[] and 1/l[].
+__host__ __device__ inline Layout layout_for(int R, int nq_s, int stages, int pb) {
     Layout L;
     L.q_off = 0;
     L.kv_off = align_up(nq_s * R * 128, 1024);
     L.p_off = L.kv_off + stages * STAGE_BYTES;
     L.misc_off = align_up(L.p_off + pb * R * NK * 2, 128);
-    L.total = L.misc_off + BAR_BYTES + 128 + 512 + 512 + (fp8 ? stages * NK * 4 : 0);
+    L.total = L.misc_off + BAR_BYTES + 128 + 512 + 512;
     return L;
 }
 
 // TMEM columns left for Q chunks (32 columns each) beside sb S buffers and O^T.
-__host__ __device__ inline int q_tmem_chunks(bool fp8, int R, int sb) {
-    const int used = sb * (fp8 ? s_cols<true>() : s_cols<false>()) + 4 * R;
+__host__ __device__ inline int q_tmem_chunks(int R, int sb) {
+    const int used = sb * NK + 4 * R;
     const int c = ((int)TMEM_COLS - used) / 32;
     return c < 0 ? 0 : (c > NCHUNK ? NCHUNK : c);
 }
@@ -136,7 +135,6 @@ struct Misc {
     volatile int* abort;
     float* alpha;
     float* rinv;
-    float* kscale;                // [stages][NK] per-key scales of the fp8 path
 };
 
 __device__ __forceinline__ Misc misc_at(uint8_t* smem, const Layout& L) {
@@ -146,7 +144,6 @@ __device__ __forceinline__ Misc misc_at(uint8_t* smem, const Layout& L) {
     m.abort = reinterpret_cast<volatile int*>(smem + L.misc_off + BAR_BYTES + 4);
     m.alpha = reinterpret_cast<float*>(smem + L.misc_off + BAR_BYTES + 128);
     m.rinv = reinterpret_cast<float*>(smem + L.misc_off + BAR_BYTES + 640);
-    m.kscale = reinterpret_cast<float*>(smem + L.misc_off + BAR_BYTES + 1152);
     return m;
 }
 
@@ -159,7 +156,7 @@ template <bool FP8, int STAGES, int NQT, int SB, int PB>
 __global__ void __launch_bounds__(block_threads<FP8>(), 1)
     verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap q_map, int R, int R_step, int raw_n) {
     constexpr int NT = block_threads<FP8>();
-    constexpr int SC = s_cols<FP8>();
+    constexpr int SC = NK;                               // TMEM columns of one S buffer
     constexpr int O_COL0 = SB * SC;
     using BR = Bars<STAGES>;
     constexpr int B_KV_FULL = BR::KV_FULL, B_KV_EMPTY = BR::KV_EMPTY, B_S_FULL = BR::S_FULL,
@@ -176,7 +173,7 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
     // append, typically): the CTAs become resident while it drains, and wait here until
     // it has completed and its writes are visible, before the first global read.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const Layout L = layout_for(R, nq_s, STAGES, PB, FP8);
+    const Layout L = layout_for(R, nq_s, STAGES, PB);
     const Misc M = misc_at(smem, L);
     const int raw_off = align_up(L.total, 128);          // fp8 path: raw_n raw slots from here
     uint8_t* p_s = smem + L.p_off;
@@ -358,16 +355,11 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
                     for (int ks = 0; ks < D_QK / 16; ++ks) {
                         const int c = ks >> 2;
                         const uint32_t ko = (uint32_t)((c * REGION + (ks & 3) * 32) >> 4);
-                        // fp8 path: latent dims (ks < 32) and rope dims accumulate separately, so
-                        // the per-key scale can multiply the latent part alone
-                        const bool rope = FP8 && ks >= D_V / 16;
-                        const uint32_t d = rope ? d_s + NK : d_s;
-                        const bool acc = rope ? ks > D_V / 16 : ks > 0;
                         if (c < nq_t) {
-                            mma_bf16_ta(d, tmem + Q_COL0 + ks * 8, dk + st16 + ko, id_qk, acc);
+                            mma_bf16_ta(d_s, tmem + Q_COL0 + ks * 8, dk + st16 + ko, id_qk, ks > 0);
                         } else {
                             const uint32_t qo = (uint32_t)(c - nq_t) * q_region16 + (uint32_t)(ks & 3) * 2;
-                            mma_bf16(d, dq + qo, dk + st16 + ko, id_qk, acc);
+                            mma_bf16(d_s, dq + qo, dk + st16 + ko, id_qk, ks > 0);
                         }
                     }
                     mma_commit(&M.bars[B_S_FULL + i % SB]);
@@ -482,7 +474,9 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
             }
         } else {
             // ---- fp8 widening: warp 6 + w widens keys 8 w .. 8 w + 7 of every tile from its raw
-            // slot into the swizzled bf16 stage layout.  lane l widens dims 16 l .. 16 l + 15:
+            // slot into the swizzled bf16 stage layout, latent values times the key's scale
+            // (V = scale_t * code, and Q K^T then needs no per-key step).  lane l widens dims
+            // 16 l .. 16 l + 15:
             // 16-byte pieces j0, j0 + 1 of region l / 4.  Lanes of odd regions store their second
             // piece first, so each store covers all eight 16-byte bank groups (four lanes each)
             // instead of four.
@@ -506,14 +500,16 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
                     const int f = it * 32 + lane;
                     rope[it] = *reinterpret_cast<const uint4*>(rb + RAW_ROPE + (8 * w + (f >> 3)) * 128 + (f & 7) * 16);
                 }
-                const float ksc = lane < 8 ? *reinterpret_cast<const float*>(rb + RAW_SCALE + (8 * w + lane) * 4) : 0.f;
+                const float4 ks0 = *reinterpret_cast<const float4*>(rb + RAW_SCALE + 8 * w * 4);
+                const float4 ks1 = *reinterpret_cast<const float4*>(rb + RAW_SCALE + 8 * w * 4 + 16);
+                const float ksc[8] = {ks0.x, ks0.y, ks0.z, ks0.w, ks1.x, ks1.y, ks1.z, ks1.w};
                 uint8_t* sbase = smem + L.kv_off + st * STAGE_BYTES;
 #pragma unroll
                 for (int it = 0; it < 8; ++it) {
                     const int key = 8 * w + it;
                     const uint4 r = odd ? make_uint4(raw[it].z, raw[it].w, raw[it].x, raw[it].y) : raw[it];
                     uint4 first, second;
-                    e4m3x16_to_bf16(r, first, second);
+                    e4m3x16_to_bf16_scaled(r, ksc[it], first, second);
                     uint8_t* row = sbase + region * REGION + key * 128;
                     *reinterpret_cast<uint4*>(row + (((j0 + odd) ^ (key & 7)) << 4)) = first;
                     *reinterpret_cast<uint4*>(row + (((j0 + 1 - odd) ^ (key & 7)) << 4)) = second;
@@ -524,7 +520,6 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
                     const int key = 8 * w + (f >> 3), cc = f & 7;
                     *reinterpret_cast<uint4*>(sbase + 8 * REGION + key * 128 + ((cc ^ (key & 7)) << 4)) = rope[it];
                 }
-                if (lane < 8) M.kscale[st * NK + 8 * w + lane] = ksc;
                 fence_proxy_async_smem();                         // generic stores -> tensor-core reads
                 if (!(a.debug_stall && i == 0)) mbar_arrive(&M.bars[B_KV_FULL + st]);
                 __syncwarp();                                     // raw slot read by the whole warp
@@ -590,26 +585,7 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
             tc_fence_after();
             uint32_t sv[NK];
             tmem_ld32(tmem + lane_base + (i % SB) * SC, sv);
-            float ksc[FP8 ? NK : 1];
-            if constexpr (FP8) {
-                // s = scale * (scale_t * q_lat . k8 + q_rope . k_rope)
-                uint32_t sr[NK];
-                tmem_ld32(tmem + lane_base + (i % SB) * SC + NK, sr);
-                tmem_ld_wait();
-                // the key scales were written before the tile's kv_full arrival
-                ok = mbar_wait(&M.bars[B_KV_FULL + i % STAGES], (i / STAGES) & 1, M.abort);
-                const float4* ks4 = reinterpret_cast<const float4*>(M.kscale + (i % STAGES) * NK);
-#pragma unroll
-                for (int k4 = 0; k4 < NK / 4; ++k4) {
-                    const float4 v = ks4[k4];
-                    ksc[4 * k4] = v.x; ksc[4 * k4 + 1] = v.y; ksc[4 * k4 + 2] = v.z; ksc[4 * k4 + 3] = v.w;
-                }
-#pragma unroll
-                for (int k = 0; k < NK; ++k)
-                    sv[k] = __float_as_uint(ksc[k] * __uint_as_float(sv[k]) + __uint_as_float(sr[k]));
-            } else {
-                tmem_ld_wait();
-            }
+            tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&M.bars[B_S_FREE + i % SB]);
 
@@ -671,9 +647,7 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
             for (int k = 0; k < NK; k += 2) {
                 const float p0 = exp2f(x[k] - mu), p1 = exp2f(x[k + 1] - mu);
                 ladd += p0 + p1;                        // the row sum keeps fp32 probabilities
-                // fp8 path: V = scale_t * e4m3 code, so P V = (P scale_t) code
-                const float f0 = FP8 ? p0 * ksc[k] : p0, f1 = FP8 ? p1 * ksc[FP8 ? k + 1 : 0] : p1;
-                __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+                __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
                 pk[k / 2] = *reinterpret_cast<uint32_t*>(&h);
             }
             l += ladd;
@@ -758,8 +732,8 @@ constexpr int MAX_SMEM = 232448;                     // opt-in shared memory per
 
 // Instantiations: (fp8, key stages, Q chunks in TMEM, S buffers, P buffers).  bf16 up to
 // 80 rows: five stages with one S and one P buffer and five Q chunks in TMEM; at 96 rows
-// three stages, two chunks in TMEM.  fp8 (one S buffer): six chunks up to 64 rows, four
-// at 80, three bf16 stages so that two to four raw slots fit beside them.
+// three stages, two chunks in TMEM.  fp8 (one S buffer): seven chunks up to 64 rows,
+// five at 80, three bf16 stages so that three or four raw slots fit beside them.
 template <bool FP8, int STAGES, int NQT, int SB, int PB>
 cudaError_t launch_one(bool set_attr, dim3 grid, cudaStream_t stream, const VerifyArgs& a, const CUtensorMap& q_map,
                        int R, int R_step) {
@@ -768,8 +742,8 @@ cudaError_t launch_one(bool set_attr, dim3 grid, cudaStream_t stream, const Veri
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SMEM);
         if (e != cudaSuccess) return e;
     }
-    if (q_tmem_chunks(FP8, R, SB) < NQT) return cudaErrorInvalidConfiguration;
-    int smem = layout_for(R, NCHUNK - NQT, STAGES, PB, FP8).total;
+    if (q_tmem_chunks(R, SB) < NQT) return cudaErrorInvalidConfiguration;
+    int smem = layout_for(R, NCHUNK - NQT, STAGES, PB).total;
     int raw_n = 0;
     if (FP8) {                                       // as many raw slots as still fit
         smem = align_up(smem, 128);
@@ -804,8 +778,8 @@ cudaError_t launch_verify_tc(const VerifyArgs& a_in, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     int n_tiles, R_step, R;
-    // fp8: at 96 rows no TMEM is left for Q and the shared-memory Q tile, the key stages
-    // and two P buffers exceed the opt-in limit, so its tiles stop at 80 rows
+    // fp8: at 96 rows a single raw slot would fit beside the shared-memory Q tile, the
+    // key stages and two P buffers, so its tiles stop at 80 rows
     tc_tiling(a.q_len * a.H, a.kv_fp8 ? 80 : MAX_R, &n_tiles, &R_step, &R);
     CUtensorMap q_map;
     const uint64_t q_rows = (uint64_t)a.B * a.q_len * a.H;
@@ -815,13 +789,13 @@ cudaError_t launch_verify_tc(const VerifyArgs& a_in, cudaStream_t stream) {
     dim3 grid(a.nsplit, n_tiles, a.balanced ? 1 : a.B);
     int which;
     if (!a.kv_fp8) which = R <= 80 ? 0 : 1;
-    else which = q_tmem_chunks(true, R, 1) >= 6 ? 2 : 3;
+    else which = q_tmem_chunks(R, 1) >= 7 ? 2 : 3;
     const bool set = !attr_set[dev][which];
     switch (which) {
         case 0: e = launch_one<false, 5, 5, 1, 1>(set, grid, stream, a, q_map, R, R_step); break;
         case 1: e = launch_one<false, 3, 2, 2, 2>(set, grid, stream, a, q_map, R, R_step); break;
-        case 2: e = launch_one<true, 3, 6, 1, 2>(set, grid, stream, a, q_map, R, R_step); break;
-        case 3: e = launch_one<true, 3, 4, 1, 2>(set, grid, stream, a, q_map, R, R_step); break;
+        case 2: e = launch_one<true, 3, 7, 1, 2>(set, grid, stream, a, q_map, R, R_step); break;
+        case 3: e = launch_one<true, 3, 5, 1, 2>(set, grid, stream, a, q_map, R, R_step); break;
         default: e = cudaErrorInvalidConfiguration; break;
     }
     if (e == cudaSuccess) attr_set[dev][which] = true;

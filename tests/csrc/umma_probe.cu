@@ -13,7 +13,8 @@
 //   2-D tile copies (box 64 columns x R rows, 128-byte swizzle) into nine regions of
 //   R x 128 B; the raw shared-memory bytes are copied out.
 // fp8_decode_probe: the fp8 key path's e4m3 -> bf16 decoder applied to n codes (n a
-//   multiple of 16), sixteen per thread, bf16 bit patterns out.
+//   multiple of 16), sixteen per thread, bf16 bit patterns out; with scales, the scaled
+//   decoder of the widening warps, group i of sixteen codes times scales[i].
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -181,6 +182,15 @@ __global__ void fp8_decode_kernel(const uint4* codes, uint4* out, int groups) {
     out[2 * i + 1] = hi;
 }
 
+__global__ void fp8_decode_scaled_kernel(const uint4* codes, const float* scales, uint4* out, int groups) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= groups) return;
+    uint4 lo, hi;
+    mla::e4m3x16_to_bf16_scaled(codes[i], scales[i], lo, hi);
+    out[2 * i] = lo;
+    out[2 * i + 1] = hi;
+}
+
 }  // namespace
 
 // codes: n e4m3 bytes, out: n bf16 bit patterns; both device pointers, 16-byte aligned
@@ -189,6 +199,16 @@ extern "C" int fp8_decode_probe(const uint8_t* codes, uint16_t* out, int n, cuda
     const int groups = n / 16;
     fp8_decode_kernel<<<(groups + 127) / 128, 128, 0, stream>>>(reinterpret_cast<const uint4*>(codes),
                                                                reinterpret_cast<uint4*>(out), groups);
+    return cudaGetLastError() == cudaSuccess ? 0 : -6;
+}
+
+// as fp8_decode_probe, codes of group i (sixteen codes) times scales[i] (n / 16 floats)
+extern "C" int fp8_decode_scaled_probe(const uint8_t* codes, const float* scales, uint16_t* out, int n,
+                                       cudaStream_t stream) {
+    if (n <= 0 || n % 16 || ((uintptr_t)codes | (uintptr_t)out) % 16 || (uintptr_t)scales % 4) return -2;
+    const int groups = n / 16;
+    fp8_decode_scaled_kernel<<<(groups + 127) / 128, 128, 0, stream>>>(
+        reinterpret_cast<const uint4*>(codes), scales, reinterpret_cast<uint4*>(out), groups);
     return cudaGetLastError() == cudaSuccess ? 0 : -6;
 }
 

@@ -37,6 +37,8 @@ def probe():
     L.tma_tile_probe.restype = I
     L.fp8_decode_probe.argtypes = [P, P, I, P]
     L.fp8_decode_probe.restype = I
+    L.fp8_decode_scaled_probe.argtypes = [P, P, P, I, P]
+    L.fp8_decode_scaled_probe.restype = I
     return L
 
 
@@ -139,3 +141,41 @@ def test_fp8_decode_every_code_every_position(probe):
     assert nan.sum() > 0 and np.array_equal(np.isnan(got), nan)
     assert np.array_equal(got[~nan], want[~nan])
     assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))    # -0 stays -0
+
+
+def _bf16_rne_bits(x32: np.ndarray) -> np.ndarray:
+    """IEEE fp32 -> bf16 bit patterns, round to nearest even (finite and infinite inputs)."""
+    b = x32.view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_fp8_decode_scaled(probe):
+    """The widening warps' decoder: each value is the IEEE fp32 product code * scale rounded
+    to the nearest bf16 (ties to even), bit for bit; NaN codes stay NaN and -0 stays -0."""
+    import oracle
+    rng = np.random.default_rng(6)
+    base = np.arange(256, dtype=np.uint8)
+    codes = np.concatenate([np.concatenate([np.roll(base, k) for k in range(16)]),
+                            rng.integers(0, 256, size=4096 * 16, dtype=np.uint8)])
+    groups = codes.size // 16
+    scales = rng.uniform(0.5, 2.0, size=groups).astype(np.float32)       # the workloads' range
+    scales[::7] = np.float32(2.0) ** rng.integers(-8, 9, size=scales[::7].size)
+    scales[3::11] = rng.uniform(1e-4, 1e-2, size=scales[3::11].size).astype(np.float32)
+    scales[5::13] = rng.uniform(1e2, 1e4, size=scales[5::13].size).astype(np.float32)
+    dev = torch.device("cuda", 0)
+    c = torch.from_numpy(codes).to(dev)
+    sc = torch.from_numpy(scales).to(dev)
+    out = torch.empty(codes.size, dtype=torch.int16, device=dev)
+    assert probe.fp8_decode_scaled_probe(c.data_ptr(), sc.data_ptr(), out.data_ptr(), codes.size, None) == 0
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint16)
+    val = oracle.e4m3_to_f64(codes)
+    nan = np.isnan(val)
+    prod = val[~nan].astype(np.float32) * np.repeat(scales, 16)[~nan]     # IEEE fp32 product
+    assert nan.sum() > 0
+    assert np.all((got[nan] & 0x7FFF) > 0x7F80)                            # NaN
+    assert np.array_equal(got[~nan], _bf16_rne_bits(prod))
+    # within a relative 2^-8 (half a bf16 ulp) of the exact dequantised value
+    back = (got[~nan].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    exact = val[~nan] * np.repeat(scales, 16)[~nan].astype(np.float64)
+    assert np.all(np.abs(back - exact) <= np.abs(exact) * (2.0 ** -8 + 2.0 ** -23))

@@ -182,17 +182,49 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.y;
     int s = blockIdx.x, b = blockIdx.z;
+    const int rows = a.q_len * a.H;
+    const int row0 = g * R_step;
+    const int nrows = min(R_step, rows - row0);
+    // the swizzled layouts need a 1024-byte aligned base: otherwise report and do no work
+    const bool misaligned = (smem_u32(smem) & 1023u) != 0;
+    const bool balanced = !FP8 && a.balanced;
+    // Q-to-TMEM warps: the first NQ0 chunks of Q row r (rows past the tile: zeros)
+    uint4 qraw[4 * 8];
+    auto load_q0 = [&]() {
+        const int r = (warp & 3) * 32 + lane;
+        const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * rows + row0 + r) * D_QK);
+#pragma unroll
+        for (int j = 0; j < 8 * NQ0; ++j)
+            qraw[j] = r < nrows ? __ldg(qrow + j) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    // With the stream known from the grid (not balanced), the cold reads that need no length
+    // go out before seq_lens[b] is read: the Q-to-TMEM warps' first chunks of Q and, since
+    // streams usually fill their table row (n == slot_stride), the gather warps' slot
+    // indices of their first two groups of tiles for the split range that length gives
+    // (kept when the real range is the same; the indices read stay inside the stream's
+    // table row).
+    int spec_cur = 0, spec_nxt = 0, spec_gb = -1, spec_ge = -1;
+    if (!balanced) {
+        if (!FP8 && warp >= 6) {
+            split_range(a.slot_stride, a.nsplit, s, NK, &spec_gb, &spec_ge);
+            const int Tg = (spec_ge - spec_gb + NK - 1) / NK;
+            const int32_t* srow = a.slot + (int64_t)b * a.slot_stride;
+            const int key = 8 * (warp - 6) + (lane & 7);
+            const int t0 = lane >> 3;
+            if (t0 < Tg) spec_cur = __ldg(srow + min(spec_gb + t0 * NK + key, spec_ge - 1));
+            if (t0 + 4 < Tg) spec_nxt = __ldg(srow + min(spec_gb + (t0 + 4) * NK + key, spec_ge - 1));
+        } else if (warp >= 2 && warp < 6 && !misaligned && nq_t > 0) {
+            load_q0();
+        }
+    }
     int bal_chunk = 0;
-    if (!FP8 && a.balanced) {
+    if (balanced) {
         // one grid of split slots shared by all streams (every warp finds the same slot)
         const BalancedPlan P = balanced_plan(a.seq_lens, a.B, a.q_len, a.slot_stride, a.bal_G);
         balanced_slot(P, blockIdx.x, &b, &s);
         if (b < 0) return;                               // slot beyond the streams' need: no work
         bal_chunk = P.chunk;
     }
-    const int rows = a.q_len * a.H;
-    const int row0 = g * R_step;
-    const int nrows = min(R_step, rows - row0);
     const int n = FP8 ? a.slot_stride : a.seq_lens[b];
     const bool bad_len = FP8 ? false : (n < a.q_len || n > a.slot_stride);
     int k_begin = 0, k_end = 0;
@@ -208,34 +240,14 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
     const int64_t part_row0 = (!FP8 && a.balanced) ? (int64_t)blockIdx.x * rows + row0
                                                     : ((int64_t)b * rows + row0) * a.nsplit + s;
     const int64_t part_row_step = (!FP8 && a.balanced) ? 1 : a.nsplit;
-    // the swizzled layouts need a 1024-byte aligned base: otherwise report and do no work
-    const bool misaligned = (smem_u32(smem) & 1023u) != 0;
     const int T = misaligned ? 0 : (k_end - k_begin + NK - 1) / NK;
     const int p = FP8 ? n : n - a.q_len;                 // first draft key (none on the fp8 path)
-
-    // Streams usually fill their table row (n == slot_stride): the gather warps load the
-    // slot indices of their first two groups of tiles for the split range that length
-    // gives while seq_lens[b] is still in flight, and keep them when the real range is
-    // the same.  The indices read stay inside the stream's table row.
-    int spec_cur = 0, spec_nxt = 0;
-    bool spec_ok = false;
-    if (!FP8 && !a.balanced && warp >= 6) {
-        int gb, ge;
-        split_range(a.slot_stride, a.nsplit, s, NK, &gb, &ge);
-        const int Tg = (ge - gb + NK - 1) / NK;
-        const int32_t* srow = a.slot + (int64_t)b * a.slot_stride;
-        const int key = 8 * (warp - 6) + (lane & 7);
-        const int t0 = lane >> 3;
-        if (t0 < Tg) spec_cur = __ldg(srow + min(gb + t0 * NK + key, ge - 1));
-        if (t0 + 4 < Tg) spec_nxt = __ldg(srow + min(gb + (t0 + 4) * NK + key, ge - 1));
-        spec_ok = gb == k_begin && ge == k_end;
-    }
+    const bool spec_ok = !balanced && spec_gb == k_begin && spec_ge == k_end;
 
     // ---- set-up.  Each role initialises the barriers it uses and starts its first cold
     // loads before the block-wide barrier, so Q, the slot indices and the first key rows
     // arrive in parallel instead of after it.  The gather warps only arrive at that barrier
     // (they use no TMEM) and start copying as soon as their slot indices are in.
-    uint4 qraw[4 * 8];                                   // Q-to-TMEM warps: chunks 0 .. NQ0-1 of their row
     if (warp == 0) {
         tmem_alloc(M.tmem_slot, TMEM_COLS);
         tmem_relinquish();
@@ -278,13 +290,8 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
         __syncwarp();
         bar_sync(4, NT - 32 * 6);                        // the gather warps see their barriers
         bar_arrive(3, NT);
-    } else if (!misaligned && nq_t > 0) {
-        // the first TMEM chunks of Q row r (rows past the tile: zeros)
-        const int r = (warp & 3) * 32 + lane;
-        const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * rows + row0 + r) * D_QK);
-#pragma unroll
-        for (int j = 0; j < 8 * NQ0; ++j)
-            qraw[j] = r < nrows ? __ldg(qrow + j) : make_uint4(0u, 0u, 0u, 0u);
+    } else if (balanced && !misaligned && nq_t > 0) {
+        load_q0();                                       // the stream is known only now
     }
     if (warp < 6) {
         tc_fence_before();

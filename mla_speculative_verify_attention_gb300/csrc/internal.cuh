@@ -74,6 +74,7 @@ __host__ __device__ inline void split_range(int n, int S, int s, int tile, int* 
 // i + 32), so no barrier or shared memory is needed.
 struct BalancedPlan {
     int chunk;
+    int n[2];       // lengths of streams lane and lane + 32 (0 past B)
     int ns[2];      // split slots of streams lane and lane + 32
     int incl[2];    // inclusive prefix sums of the slot counts at those streams
 };
@@ -81,7 +82,7 @@ struct BalancedPlan {
 __device__ inline BalancedPlan balanced_plan(const int32_t* seq_lens, int B, int q_len, int slot_stride, int G) {
     const int lane = threadIdx.x & 31;
     BalancedPlan P;
-    int n[2];
+    int* n = P.n;
     bool ok[2];
     long long t = 0;
 #pragma unroll
@@ -93,7 +94,8 @@ __device__ inline BalancedPlan balanced_plan(const int32_t* seq_lens, int B, int
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    long long c = (t + G - 1) / G;
+    // 32-bit divisions whenever the total fits (warp-uniform branch)
+    long long c = t < (1ll << 30) ? (long long)(((unsigned)t + (unsigned)G - 1u) / (unsigned)G) : (t + G - 1) / G;
     c = (c + 31) / 32 * 32;
     if (c < 128) c = 128;
     if (c > (1 << 30)) c = 1 << 30;
@@ -102,7 +104,7 @@ __device__ inline BalancedPlan balanced_plan(const int32_t* seq_lens, int B, int
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int i = lane + 32 * h;
-        P.ns[h] = i < B ? (ok[h] ? (int)(((long long)n[h] + c - 1) / c) : 1) : 0;
+        P.ns[h] = i < B ? (ok[h] ? (int)(((unsigned)n[h] + (unsigned)c - 1u) / (unsigned)c) : 1) : 0;
         int v = P.ns[h];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {

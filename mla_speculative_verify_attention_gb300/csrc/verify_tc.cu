@@ -217,15 +217,16 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
             load_q0();
         }
     }
-    int bal_chunk = 0;
+    int bal_chunk = 0, bal_n = 0;
     if (balanced) {
         // one grid of split slots shared by all streams (every warp finds the same slot)
         const BalancedPlan P = balanced_plan(a.seq_lens, a.B, a.q_len, a.slot_stride, a.bal_G);
         balanced_slot(P, blockIdx.x, &b, &s);
         if (b < 0) return;                               // slot beyond the streams' need: no work
         bal_chunk = P.chunk;
+        bal_n = __shfl_sync(0xffffffffu, b < 32 ? P.n[0] : P.n[1], b & 31);   // seq_lens[b], read by the plan
     }
-    const int n = FP8 ? a.slot_stride : a.seq_lens[b];
+    const int n = FP8 ? a.slot_stride : (balanced ? bal_n : a.seq_lens[b]);
     const bool bad_len = FP8 ? false : (n < a.q_len || n > a.slot_stride);
     int k_begin = 0, k_end = 0;
     if (!bad_len) {

@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
     const bool bad_len = FP8 ? false : (n < a.q_len || n > a.slot_stride);
     int k_begin = 0, k_end = 0;
     if (!bad_len) {
-        if (!FP8 && a.balanced) {
+        if (balanced) {
             k_begin = min(n, s * bal_chunk);
             k_end = (int)min((long long)n, (long long)(s + 1) * bal_chunk);
         } else {
@@ -238,9 +238,9 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
         }
     }
     // partial row of stream row rr: uniform [B * rows][nsplit] or balanced [slot][rows]
-    const int64_t part_row0 = (!FP8 && a.balanced) ? (int64_t)blockIdx.x * rows + row0
-                                                    : ((int64_t)b * rows + row0) * a.nsplit + s;
-    const int64_t part_row_step = (!FP8 && a.balanced) ? 1 : a.nsplit;
+    const int64_t part_row0 = balanced ? (int64_t)blockIdx.x * rows + row0
+                                       : ((int64_t)b * rows + row0) * a.nsplit + s;
+    const int64_t part_row_step = balanced ? 1 : a.nsplit;
     const int T = misaligned ? 0 : (k_end - k_begin + NK - 1) / NK;
     const int p = FP8 ? n : n - a.q_len;                 // first draft key (none on the fp8 path)
     const bool spec_ok = !balanced && spec_gb == k_begin && spec_ge == k_end;

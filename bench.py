@@ -5,15 +5,16 @@
 
 Prints ONE JSON line.  A step is one verify call through the C ABI
 (mla_verify_attn: split kernel + combine) over one synthetic batch of the named
-workload (default c2: 1 stream, q_len 9, H 64, prefix 4096, contiguous slots,
-causal chain -- the pages' microbenchmark shape).  `value` is effective KV
-bandwidth (KV-row bytes / time) with inputs resident in HBM, timed with CUDA
-events per step on the launching stream; L2 is flushed before every step, outside
-the events: 256 MiB are written and then another 256 MiB buffer is read, so none of
-the call's inputs is in L2 and the flush leaves no dirty line whose write-back would
-fall inside the timed call (a write-only flush is timed too and reported beside it).  The split kernel alone is timed the same way in
-a second loop (its duration is the roofline's denominator), and a warm-L2 loop
-(no flush) is reported beside it.  `e2e` is the same metric end to end: the
+workload (default c4: 8 streams, q_len 9, H 8, prefixes U{1024..46080}, slots
+scattered over a 2^20-row pool, random draft trees -- the serving shape of long
+contexts at H 8 per rank).  `value` is effective KV bandwidth (KV-row bytes /
+time) with inputs resident in HBM, timed with CUDA events per step on the
+launching stream; L2 is flushed before every step, outside the events: 256 MiB
+are written and then another 256 MiB buffer is read, so none of the call's inputs
+is in L2 and the flush leaves no dirty line whose write-back would fall inside the
+timed call (a write-only flush is timed too and reported beside it).  The split
+kernel alone is timed the same way in a second loop (its duration is the
+roofline's denominator), and a warm-L2 loop (no flush) is reported beside it.  `e2e` is the same metric end to end: the
 step's inputs (queries, slot table, lengths, mask and the new draft KV rows)
 copied from one pinned host buffer in one copy, the KV append kernel, the verify
 call and the outputs (out and lse, one buffer) copied back, all inside the timed

@@ -212,9 +212,9 @@ int mla_verify_combine(const float* part_out, const float* part_lse, int B, int 
  *     k_j = [ decode_e4m3(kv_lat[s_j, 0:512]) * kv_scale[s_j] | kv_rope[s_j, 0:64] ]
  *     v_j = decode_e4m3(kv_lat[s_j, 0:512]) * kv_scale[s_j]
  *     out[b,h] = softmax_j(scale * q[b,h] . k_j) v_j,  lse[b,h] = ln sum_j exp(...)
- * decode_e4m3 is the OCP FP8 E4M3 ("fn") value of the byte.  The kernel converts
- * codes to bf16 exactly and applies kv_scale to the latent scores and to the
- * softmax weights, so the dequantisation adds no rounding.
+ * decode_e4m3 is the OCP FP8 E4M3 ("fn") value of the byte.  The kernel dequantises
+ * each latent value once, as the fp32 product decode_e4m3(code) * kv_scale rounded to
+ * bf16 (one rounding, relative error at most 2^-8), and uses the rope dims as stored.
  *   q          bf16 [B, H, 576] (= [B, 1, H, 576]), 16-byte aligned
  *   kv_lat     uint8 [n_pool, 512] e4m3 codes, 16-byte aligned
  *   kv_scale   fp32 [n_pool]

@@ -1,7 +1,7 @@
 #!/usr/bin/env python3
 """Benchmark of MLA speculative-verify attention on one GB300 (or N replicas).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4] [--impl reference]
 
 Prints ONE JSON line.  A step is one verify call through the C ABI
 (mla_verify_attn: split kernel + combine) over one synthetic batch of the named
@@ -14,12 +14,13 @@ are written and then another 256 MiB buffer is read, so none of the call's input
 is in L2 and the flush leaves no dirty line whose write-back would fall inside the
 timed call (a write-only flush is timed too and reported beside it).  The split
 kernel alone is timed the same way in a second loop (its duration is the
-roofline's denominator), and a warm-L2 loop (no flush) is reported beside it.  `e2e` is the same metric end to end: the
-step's inputs (queries, slot table, lengths, mask and the new draft KV rows)
-copied from one pinned host buffer in one copy, the KV append kernel, the verify
-call and the outputs (out and lse, one buffer) copied back, all inside the timed
-region.  `--impl reference` times the
-fp64 CPU oracle on this host's cores instead (the reference arm).
+roofline's denominator), and a warm-L2 loop (no flush; a device-side spin covers
+the host's submission instead) is reported beside it.  `e2e` is the same metric
+end to end: the step's inputs (queries, slot table, lengths, mask and the new
+draft KV rows) copied from one pinned host buffer in one copy, the KV append
+kernel, the verify call and the outputs (out and lse, one buffer) copied back,
+all inside the timed region.  `--impl reference` times the fp64 CPU oracle on
+this host's cores instead (the reference arm).
 """
 from __future__ import annotations
 
@@ -486,20 +487,22 @@ def run_gpu(args):
         before each call (outside the events) unless flush_l2 is False (clean=False: the
         write-only flush, whose dirty lines are written back during the call).  Returns ms
         per call.
-        With the flush each step ends with a synchronize: the flush then keeps the GPU busy
-        while the host submits the call, so the events never time the GPU waiting for the
-        host (a loop that queued every step at once measured c4 at 222 us per call against
-        72 us once the host fell behind).  Without it the steps queue back to back."""
+        Each step ends with a synchronize, and the GPU is kept busy while the host submits
+        the next call -- by the flush, or without one by a ~100 us device-side spin that
+        touches no memory -- so the events never time the GPU waiting for the host (a loop
+        that queued every step at once measured c4 at 222 us per call against 72 us once the
+        host fell behind)."""
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
         torch.cuda.synchronize(dev)
         for i in range(n):
             if flush_l2:
                 flush_l2_lines(i, clean)
+            else:
+                torch.cuda._sleep(200_000)
             ev[i][0].record(stream)
             fn()
             ev[i][1].record(stream)
-            if flush_l2:
-                torch.cuda.synchronize(dev)
+            torch.cuda.synchronize(dev)
         torch.cuda.synchronize(dev)
         return [a.elapsed_time(b) for a, b in ev]
 

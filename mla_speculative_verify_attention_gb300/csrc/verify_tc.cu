@@ -164,9 +164,10 @@ __global__ void __launch_bounds__(block_threads<FP8>(), 1)
                   B_RAW_FULL = BR::RAW_FULL, B_RAW_EMPTY = BR::RAW_EMPTY;
     constexpr int nq_t = NQT;                            // Q chunks 0 .. NQT-1 live in TMEM,
     constexpr int nq_s = NCHUNK - NQT;                   // chunks NQT .. 8 in shared memory
-    // TMEM chunks loaded before the set-up barrier (an odd count leaves a pair for the loop,
-    // which keeps the register peak of the five-chunk variant below the 168 a thread gets)
-    constexpr int NQ0 = nq_t == 5 ? 3 : (nq_t < 4 ? nq_t : 4);
+    // TMEM chunks loaded before the set-up barrier (an odd count leaves pairs for the loop,
+    // which keeps the register peak of the five- and seven-chunk variants below the 168 a
+    // thread gets)
+    constexpr int NQ0 = (nq_t == 5 || nq_t == 7) ? 3 : (nq_t < 4 ? nq_t : 4);
     const int Q_COL0 = O_COL0 + 4 * R;                   // Q chunk c < nq_t: TMEM columns Q_COL0 + 32 c ..
     extern __shared__ __align__(1024) uint8_t smem[];
     // Launched as a programmatic dependent of the previous kernel on the stream (the KV

@@ -26,15 +26,15 @@
 //            128-dim chunks, fp32 accumulators resident in TMEM
 // Computing P V transposed keeps O^T in 4 x rows <= 384 TMEM columns, so the S
 // buffers (one or two of 32 columns) fit beside it in the 512-column TMEM and Q K^T
-// runs once per tile; the columns left over hold as many 32-column Q chunks as fit (5
-// up to 80 rows with one S buffer, 2 at 96 with two, 7 up to 64 rows).  Measured on GB300, an
-// M=128 x N=32 x K=16 MMA issued from a converged warp takes ~17 cycles with A in TMEM
-// and ~40 with A in shared memory (bound by shared-memory reads of the 4 KB A tile),
-// so every Q chunk moved to TMEM takes four MMAs off the shared-memory port, and the
-// freed shared memory buys key stages: five for up to 80 bf16 rows (one P buffer),
-// three at 96 rows and on the fp8 path.  The same swizzled key stage is the K-major B
-// operand of Q K^T and the M-major A operand of V^T P^T (V = first 512 dims of each key
-// row).
+// runs once per tile; the columns left over hold as many 32-column Q chunks as fit
+// (bf16: 5 up to 80 rows with one S buffer, 2 at 96 with two; fp8: 7 up to 64 rows, 5
+// at 80).  Measured on GB300, an M=128 x N=32 x K=16 MMA issued from a converged warp
+// takes ~17 cycles with A in TMEM and ~40 with A in shared memory (bound by
+// shared-memory reads of the 4 KB A tile), so every Q chunk moved to TMEM takes four MMAs
+// off the shared-memory port, and the freed shared memory buys key stages: five for up
+// to 80 bf16 rows (one P buffer), three at 96 rows and on the fp8 path.  The same
+// swizzled key stage is the K-major B operand of Q K^T and the M-major A operand of
+// V^T P^T (V = first 512 dims of each key row).
 //
 // Warp roles (320 threads; 384 on the fp8 path):
 //   warp 0      TMEM allocation; Q K^T issue loop run by the whole warp (operands stay
